@@ -1,0 +1,354 @@
+"""Pins for the fp64 oracle: closed forms, special cases that reduce to library
+routines, invariants and exact index-handling checks.  CPU only.
+
+Each test fixes something the pages and the mathematics determine without
+re-typing the oracle's own loop:
+  * dense special case  -> scipy softmax / logsumexp over a numpy matmul
+  * q = 0               -> out is the mean of the selected V rows, lse = ln(k_valid)
+  * one valid entry     -> out is that V row, lse = scale * <q, K>
+  * equal scores        -> uniform weights (pins the rope columns' role in K)
+  * paging, padding, index order, shard split + merge, merge order -> invariances
+  * one-hot V rows      -> the exact multiset of rows read
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+import oracle
+from tests._problems import D_QK, D_V, Paged, bf16_bits, bits_to_f64, rng_normal
+
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+def problem(dense, seq_lens, q, topk, Q=1, bs=64, perm_seed=None, fill=0.0, spare=0):
+    pg = Paged(np.asarray(dense, np.float32), seq_lens, bs, perm_seed, spare, fill)
+    q_bits = bf16_bits(q)
+    prob = oracle.Problem(q_bits, pg.kv, pg.block_table, pg.seq_lens,
+                          np.asarray(topk, dtype=np.int32), Q, SCALE)
+    return prob, pg
+
+
+def bf(x):
+    """Values as the oracle sees them: rounded to bf16, widened to float64."""
+    return bits_to_f64(bf16_bits(x))
+
+
+# --------------------------------------------------------------------------------------
+# special case: every position selected == dense softmax attention (library routines)
+# --------------------------------------------------------------------------------------
+@pytest.mark.parametrize("S,bs,perm", [(200, 64, None), (130, 16, 3), (64, 64, 5)])
+def test_dense_equals_library_softmax_attention(S, bs, perm):
+    B, h = 2, 3
+    dense = rng_normal((B, S, D_QK), 1)
+    q = rng_normal((B, h, D_QK), 2)
+    topk = np.tile(np.arange(S, dtype=np.int32), (B, 1))
+    prob, _ = problem(dense, [S] * B, q, topk, bs=bs, perm_seed=perm)
+    out, lse = oracle.decode(prob)
+    K = bf(dense)
+    Qm = bf(q)
+    for b in range(B):
+        s = SCALE * (Qm[b] @ K[b].T)                    # [h, S]
+        ref_out = softmax(s, axis=1) @ K[b][:, :D_V]    # V = latent columns
+        np.testing.assert_allclose(out[b], ref_out, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(lse[b], logsumexp(s, axis=1), rtol=1e-13, atol=1e-12)
+
+
+# --------------------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------------------
+def test_zero_query_gives_mean_of_selected_rows_and_ln_k():
+    B, S, h = 2, 300, 2
+    dense = rng_normal((B, S, D_QK), 11)
+    q = np.zeros((B, h, D_QK), np.float32)
+    rng = np.random.default_rng(12)
+    sel = [rng.choice(S, size=37, replace=False), rng.choice(S, size=5, replace=False)]
+    topk = np.full((B, 40), -1, np.int32)
+    for b in range(B):
+        topk[b, : len(sel[b])] = sel[b]
+    prob, _ = problem(dense, [S] * B, q, topk, perm_seed=9)
+    out, lse = oracle.decode(prob)
+    K = bf(dense)
+    for b in range(B):
+        for hh in range(h):
+            np.testing.assert_allclose(out[b, hh], K[b, sel[b], :D_V].mean(axis=0), rtol=0, atol=1e-14)
+            assert lse[b, hh] == pytest.approx(math.log(len(sel[b])), abs=1e-15)
+
+
+def test_single_entry_gives_that_row_and_its_scaled_score():
+    S, h = 128, 4
+    dense = rng_normal((1, S, D_QK), 21)
+    q = rng_normal((1, h, D_QK), 22)
+    p = 77
+    topk = np.array([[-1, p, -1, 500]], np.int32)  # 500 is outside the cache: padding
+    prob, _ = problem(dense, [S], q, topk, perm_seed=1)
+    out, lse = oracle.decode(prob)
+    K = bf(dense)[0, p]
+    Qm = bf(q)[0]
+    for hh in range(h):
+        np.testing.assert_array_equal(out[0, hh], K[:D_V])
+        assert lse[0, hh] == pytest.approx(SCALE * float(Qm[hh] @ K), rel=1e-14, abs=1e-14)
+
+
+def test_equal_rope_scores_give_uniform_weights():
+    # q lives only in the rope columns and every row has the same rope part, so
+    # every score is equal: out = mean of the latent rows, lse = s + ln(n).
+    S, h, n = 256, 2, 50
+    dense = rng_normal((1, S, D_QK), 31)
+    rope = rng_normal((D_QK - D_V,), 32)
+    dense[0, :, D_V:] = rope
+    q = np.zeros((1, h, D_QK), np.float32)
+    q[0, :, D_V:] = rng_normal((h, D_QK - D_V), 33)
+    sel = np.random.default_rng(34).choice(S, size=n, replace=False)
+    prob, _ = problem(dense, [S], q, sel[None, :], perm_seed=2)
+    out, lse = oracle.decode(prob)
+    K = bf(dense)[0]
+    Qm = bf(q)[0]
+    for hh in range(h):
+        s = SCALE * float(Qm[hh, D_V:] @ bf(rope))
+        np.testing.assert_allclose(out[0, hh], K[sel, :D_V].mean(axis=0), rtol=0, atol=1e-13)
+        assert lse[0, hh] == pytest.approx(s + math.log(n), abs=1e-13)
+
+
+def test_rope_columns_enter_the_score_but_not_the_output():
+    # latent part zero: out must be 0 while lse depends on the rope columns only
+    S, h = 64, 2
+    dense = np.zeros((1, S, D_QK), np.float32)
+    dense[0, :, D_V:] = rng_normal((S, D_QK - D_V), 41)
+    q = rng_normal((1, h, D_QK), 42)
+    sel = np.arange(0, S, 3)
+    prob, _ = problem(dense, [S], q, sel[None, :])
+    out, lse = oracle.decode(prob)
+    assert np.all(out == 0.0)
+    s = SCALE * (bf(q)[0][:, D_V:] @ bf(dense)[0, sel, D_V:].T)
+    np.testing.assert_allclose(lse[0], logsumexp(s, axis=1), rtol=1e-14)
+
+
+def test_duplicate_entries_count_once_per_list_entry():
+    S = 64
+    dense = rng_normal((1, S, D_QK), 51)
+    q = np.zeros((1, 1, D_QK), np.float32)
+    prob, _ = problem(dense, [S], q, np.array([[3, 3, 7, -1]], np.int32))
+    out, lse = oracle.decode(prob)
+    K = bf(dense)[0]
+    np.testing.assert_allclose(out[0, 0], (2 * K[3, :D_V] + K[7, :D_V]) / 3, atol=1e-14)
+    assert lse[0, 0] == pytest.approx(math.log(3), abs=1e-15)
+
+
+def test_empty_selection_gives_zero_and_minus_inf():
+    S = 64
+    dense = rng_normal((1, S, D_QK), 61)
+    q = rng_normal((1, 2, D_QK), 62)
+    prob, _ = problem(dense, [S], q, np.array([[-1, 64, 1000, -7]], np.int32))
+    out, lse = oracle.decode(prob)
+    assert np.all(out == 0.0)
+    assert np.all(np.isneginf(lse))
+
+
+def test_mtp_query_tokens_see_their_own_causal_range():
+    # Q=2: token 0 sees [0, L-1), token 1 sees [0, L)
+    L = 100
+    dense = rng_normal((1, L, D_QK), 71)
+    q = np.zeros((2, 1, D_QK), np.float32)
+    topk = np.array([[L - 1, 0, 5], [L - 1, 0, 5]], np.int32)
+    prob, _ = problem(dense, [L], q, topk, Q=2)
+    out, lse = oracle.decode(prob)
+    K = bf(dense)[0]
+    np.testing.assert_allclose(out[0, 0], K[[0, 5], :D_V].mean(axis=0), atol=1e-14)
+    np.testing.assert_allclose(out[1, 0], K[[L - 1, 0, 5], :D_V].mean(axis=0), atol=1e-14)
+    assert lse[0, 0] == pytest.approx(math.log(2))
+    assert lse[1, 0] == pytest.approx(math.log(3))
+
+
+# --------------------------------------------------------------------------------------
+# exact index handling
+# --------------------------------------------------------------------------------------
+def test_one_hot_rows_recover_the_exact_multiset_read():
+    # q = 0 and latent row of position p = one-hot at column p % 512: out * n counts
+    # how often each residue was read.  Every unselected row (and every padding
+    # target) is NaN, so a stray read would poison the output.
+    B, S = 2, 1024
+    dense = np.full((B, S, D_QK), np.nan, np.float32)
+    rng = np.random.default_rng(81)
+    topk = np.full((B, 300), -1, np.int32)
+    expected = np.zeros((B, D_V))
+    for b in range(B):
+        pos = rng.choice(S, size=256, replace=False)
+        pos = pos[np.unique(pos % D_V, return_index=True)[1]][:200]
+        for p in pos:
+            dense[b, p] = 0.0
+            dense[b, p, p % D_V] = 1.0
+            expected[b, p % D_V] += 1
+        topk[b, : len(pos)] = pos
+        topk[b, len(pos):len(pos) + 20] = rng.integers(S, 4 * S, size=20)  # out of range
+    q = np.zeros((B, 3, D_QK), np.float32)
+    prob, _ = problem(dense, [S] * B, q, topk, perm_seed=4, fill=np.nan, spare=3)
+    out, lse = oracle.decode(prob)
+    for b in range(B):
+        n = expected[b].sum()
+        for hh in range(3):
+            assert np.all(np.isfinite(out[b, hh]))
+            np.testing.assert_array_equal(np.rint(out[b, hh] * n), expected[b])
+            assert lse[b, hh] == pytest.approx(math.log(n))
+
+
+def test_nan_in_unselected_rows_does_not_leak():
+    B, S, h = 1, 512, 4
+    dense = rng_normal((B, S, D_QK), 91)
+    q = rng_normal((B, h, D_QK), 92)
+    sel = np.random.default_rng(93).choice(S, size=64, replace=False)
+    clean, _ = problem(dense, [S], q, sel[None, :], perm_seed=6)
+    poisoned_dense = np.full_like(dense, np.nan)
+    poisoned_dense[0, sel] = dense[0, sel]
+    dirty, _ = problem(poisoned_dense, [S], q, sel[None, :], perm_seed=6, fill=np.nan, spare=2)
+    o1, l1 = oracle.decode(clean)
+    o2, l2 = oracle.decode(dirty)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+# --------------------------------------------------------------------------------------
+# invariances
+# --------------------------------------------------------------------------------------
+def _random_problem(seed, B=3, S=333, h=5, k=90, Q=1, perm=None, bs=64):
+    rng = np.random.default_rng(seed)
+    dense = rng.standard_normal((B, S, D_QK)).astype(np.float32)
+    q = rng.standard_normal((B * Q, h, D_QK)).astype(np.float32)
+    topk = np.stack([rng.choice(S, size=k, replace=False) for _ in range(B * Q)]).astype(np.int32)
+    return dense, q, topk
+
+
+def test_index_order_does_not_matter():
+    dense, q, topk = _random_problem(101)
+    p1, _ = problem(dense, [333] * 3, q, topk, perm_seed=1)
+    perm = np.random.default_rng(102).permutation(topk.shape[1])
+    p2, _ = problem(dense, [333] * 3, q, topk[:, perm], perm_seed=1)
+    o1, l1 = oracle.decode(p1)
+    o2, l2 = oracle.decode(p2)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=1e-13, atol=1e-13)
+
+
+def test_padding_entries_do_not_matter():
+    dense, q, topk = _random_problem(111)
+    rng = np.random.default_rng(112)
+    pad = np.concatenate([np.full((3, 10), -1), rng.integers(333, 10 ** 6, (3, 5)),
+                          rng.integers(-10 ** 6, -1, (3, 5))], axis=1).astype(np.int32)
+    mixed = np.concatenate([topk, pad], axis=1)
+    mixed = np.stack([row[np.random.default_rng(113 + i).permutation(len(row))] for i, row in enumerate(mixed)])
+    p1, _ = problem(dense, [333] * 3, q, topk)
+    p2, _ = problem(dense, [333] * 3, q, mixed)
+    o1, l1 = oracle.decode(p1)
+    o2, l2 = oracle.decode(p2)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=1e-13, atol=1e-13)
+
+
+def test_physical_block_placement_does_not_matter():
+    dense, q, topk = _random_problem(121, bs=16)
+    outs = []
+    for perm in (None, 1, 2):
+        p, _ = problem(dense, [333] * 3, q, topk, bs=16, perm_seed=perm, spare=perm or 0)
+        outs.append(oracle.decode(p))
+    for o, l in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0][0])
+        np.testing.assert_array_equal(l, outs[0][1])
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 3, 4, 8, 13])
+def test_shard_partials_merged_equal_unsplit(n_splits):
+    rng = np.random.default_rng(131)
+    B, S, h, Q = 3, 400, 4, 2
+    dense = rng.standard_normal((B, S, D_QK)).astype(np.float32)
+    seq_lens = [400, 97, 250]
+    q = rng.standard_normal((B * Q, h, D_QK)).astype(np.float32)
+    topk = np.full((B * Q, 120), -1, np.int32)
+    for t in range(B * Q):
+        L = seq_lens[t // Q]
+        sel = rng.choice(L, size=min(L, 110), replace=False)
+        topk[t, : len(sel)] = sel
+    prob, _ = problem(dense, seq_lens, q, topk, Q=Q, perm_seed=8)
+    out, lse = oracle.decode(prob)
+    op, lp = oracle.decode_splits(prob, n_splits)
+    mo, ml = oracle.merge(op, lp)
+    np.testing.assert_allclose(mo, out, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, rtol=1e-12, atol=1e-12)
+    if n_splits == 1:
+        np.testing.assert_array_equal(op[0], out)
+        np.testing.assert_array_equal(lp[0], lse)
+
+
+def test_shard_partials_closed_form_with_zero_query():
+    # q = 0: shard r's partial is the mean of its rows with lse = ln(count in shard)
+    S, n = 200, 3                    # shard width ceil(200/3) = 67
+    dense = rng_normal((1, S, D_QK), 141)
+    sel = np.array([0, 66, 67, 133, 134, 199, 150, 10], np.int32)
+    prob, _ = problem(dense, [S], np.zeros((1, 2, D_QK), np.float32), sel[None, :])
+    op, lp = oracle.decode_splits(prob, n)
+    K = bf(dense)[0]
+    shards = [[0, 66, 10], [67, 133], [134, 199, 150]]
+    for r in range(n):
+        np.testing.assert_allclose(op[r, 0, 0], K[shards[r], :D_V].mean(axis=0), atol=1e-14)
+        assert lp[r, 0, 0] == pytest.approx(math.log(len(shards[r])))
+    mo, ml = oracle.merge(op, lp)
+    np.testing.assert_allclose(mo[0, 0], K[sel, :D_V].mean(axis=0), atol=1e-14)
+    assert ml[0, 0] == pytest.approx(math.log(len(sel)))
+
+
+def test_empty_shards_are_zero_and_minus_inf():
+    S = 256
+    dense = rng_normal((1, S, D_QK), 151)
+    sel = np.array([[200, 201, 255]], np.int32)   # all in the last of 4 shards of 64
+    prob, _ = problem(dense, [S], rng_normal((1, 1, D_QK), 152), sel)
+    op, lp = oracle.decode_splits(prob, 4)
+    for r in range(3):
+        assert np.all(op[r] == 0) and np.all(np.isneginf(lp[r]))
+    assert np.isfinite(lp[3]).all()
+
+
+def test_merge_identity_order_and_empty_partials():
+    rng = np.random.default_rng(161)
+    op = rng.standard_normal((4, 6, D_V))
+    lp = rng.standard_normal((4, 6)) * 3
+    lp[1, 2] = -np.inf
+    lp[:, 5] = -np.inf                                 # a row with no data at all
+    one_o, one_l = oracle.merge(op[:1], lp[:1])
+    np.testing.assert_array_equal(one_o[:5], op[0, :5])     # identity on rows with data
+    np.testing.assert_array_equal(one_l, lp[0])
+    assert np.all(one_o[5] == 0)                              # an empty partial carries no output
+    mo, ml = oracle.merge(op, lp)
+    perm = [2, 0, 3, 1]
+    po, pl = oracle.merge(op[perm], lp[perm])
+    np.testing.assert_allclose(po, mo, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(pl, ml, rtol=1e-14, atol=1e-14)
+    assert np.all(mo[5] == 0) and np.isneginf(ml[5])
+    # closed form: lse = logsumexp over partials, weights = softmax of the lse
+    w = softmax(lp[:, :5], axis=0)
+    np.testing.assert_allclose(ml[:5], logsumexp(lp[:, :5], axis=0), rtol=1e-14)
+    np.testing.assert_allclose(mo[:5], np.einsum("rx,rxc->xc", w, op[:, :5]), rtol=1e-12, atol=1e-13)
+
+
+def test_thread_count_does_not_change_results():
+    dense, q, topk = _random_problem(171, B=4, h=8)
+    prob, _ = problem(dense, [333] * 4, q, topk, perm_seed=3)
+    o1, l1 = oracle.decode(prob, nthreads=1)
+    o7, l7 = oracle.decode(prob, nthreads=7)
+    np.testing.assert_array_equal(o1, o7)
+    np.testing.assert_array_equal(l1, l7)
+
+
+def test_sampled_pairs_match_full_decode():
+    dense, q, topk = _random_problem(181, B=3, h=6, Q=1)
+    prob, _ = problem(dense, [333] * 3, q, topk, perm_seed=5)
+    out, lse = oracle.decode(prob)
+    t = np.array([0, 2, 1, 2])
+    hh = np.array([5, 0, 3, 3])
+    so, sl = oracle.decode_sampled(prob, t, hh)
+    np.testing.assert_array_equal(so, out[t, hh])
+    np.testing.assert_array_equal(sl, lse[t, hh])
+    op, lp = oracle.decode_splits(prob, 3)
+    r = np.array([0, 2, 1, 1])
+    so, sl = oracle.decode_sampled(prob, t, hh, shards=r, n_splits=3)
+    np.testing.assert_array_equal(so, op[r, t, hh])
+    np.testing.assert_array_equal(sl, lp[r, t, hh])
