@@ -44,25 +44,29 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(path: str):
+    """Open a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    common = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double]
+    lib.sfa_oracle_decode.argtypes = common + [P, P, I]
+    lib.sfa_oracle_decode.restype = I
+    lib.sfa_oracle_decode_splits.argtypes = common + [I, P, P, I]
+    lib.sfa_oracle_decode_splits.restype = I
+    lib.sfa_oracle_decode_sampled.argtypes = common + [I, ctypes.c_long, P, P, P, P, P, I]
+    lib.sfa_oracle_decode_sampled.restype = I
+    lib.sfa_oracle_merge.argtypes = [P, P, I, ctypes.c_long, I, P, P]
+    lib.sfa_oracle_merge.restype = I
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        I = ctypes.c_int
-        common = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double]
-        lib.sfa_oracle_decode.argtypes = common + [P, P, I]
-        lib.sfa_oracle_decode.restype = I
-        lib.sfa_oracle_decode_splits.argtypes = common + [I, P, P, I]
-        lib.sfa_oracle_decode_splits.restype = I
-        lib.sfa_oracle_decode_sampled.argtypes = common + [I, ctypes.c_long, P, P, P, P, P, I]
-        lib.sfa_oracle_decode_sampled.restype = I
-        lib.sfa_oracle_merge.argtypes = [P, P, I, ctypes.c_long, I, P, P]
-        lib.sfa_oracle_merge.restype = I
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _bind(build())
+        return _lib
 
 
 def _ptr(a):

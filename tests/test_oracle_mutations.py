@@ -1,0 +1,74 @@
+"""Plant plausible mistakes in a temporary copy of the oracle and check that the
+pins in test_oracle_pins.py catch every one of them.  CPU only.
+
+Each mutant is the oracle's C source with one textual edit, compiled with gcc
+into a temporary directory and swapped in for the duration of one check.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sfa_oracle.c")
+
+# (name, original text, planted text, pins expected to catch it)
+MUTANTS = [
+    ("dropped_scale", "double s = p->scale * dot;", "double s = dot;",
+     [pins.test_single_entry_gives_that_row_and_its_scaled_score]),
+    ("log2_lse", "*lse_out = m + log(l);", "*lse_out = m + log2(l);",
+     [pins.test_zero_query_gives_mean_of_selected_rows_and_ln_k]),
+    ("v_from_rope_side", "out_row[c] += w * bf16_to_double(vrow[c]);",
+     "out_row[c] += w * bf16_to_double(vrow[c + 64]);",
+     [pins.test_zero_query_gives_mean_of_selected_rows_and_ln_k]),
+    ("score_skips_rope", "for (int d = 0; d < p->D; ++d) dot +=",
+     "for (int d = 0; d < p->DV; ++d) dot +=",
+     [pins.test_rope_columns_enter_the_score_but_not_the_output]),
+    ("causal_off_by_one", "return (long)p->seq_lens[b] - (long)(p->Q - 1 - i);",
+     "return (long)p->seq_lens[b] - (long)(p->Q - i);",
+     [pins.test_mtp_query_tokens_see_their_own_causal_range]),
+    ("slot_ignores_table", "return phys * p->block_size + pos % p->block_size;",
+     "return (long)b * p->max_blocks_per_seq * p->block_size + pos;",
+     [pins.test_physical_block_placement_does_not_matter]),
+    ("slot_offset_swapped", "return phys * p->block_size + pos % p->block_size;",
+     "return phys * p->block_size + (pos / p->block_size) % p->block_size;",
+     [pins.test_one_hot_rows_recover_the_exact_multiset_read]),
+    ("shard_floor", "long c = S > 0 ? (S + n - 1) / n : 0;", "long c = S > 0 ? S / n : 0;",
+     [pins.test_shard_partials_closed_form_with_zero_query]),
+    ("merge_weight_sign", "double w = exp(lse_part[(size_t)r * rows + x] - L);",
+     "double w = exp(L - lse_part[(size_t)r * rows + x]);",
+     [pins.test_merge_identity_order_and_empty_partials]),
+    ("no_dedup_semantics", "long pos = idx[j];\n    if (pos < lo || pos >= hi) continue;",
+     "long pos = idx[j];\n    if (pos < lo || pos >= hi) continue;\n    if (j > 0 && idx[j - 1] == pos) continue;",
+     [pins.test_duplicate_entries_count_once_per_list_entry]),
+    ("padding_minus_one_only", "if (pos < lo || pos >= hi) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
+     "if (pos == -1) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
+     [pins.test_empty_selection_gives_zero_and_minus_inf]),
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new)  # every occurrence: both passes over the list
+    c_path = tmp_path / f"{name}.c"
+    so_path = tmp_path / f"lib{name}.so"
+    c_path.write_text(mutated)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", str(c_path),
+                    "-o", str(so_path), "-lm"], check=True)
+    return oracle._bind(str(so_path))
+
+
+@pytest.mark.parametrize("name,old,new,catchers", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, monkeypatch, name, old, new, catchers):
+    lib = _build_mutant(tmp_path, name, old, new)
+    monkeypatch.setattr(oracle, "_lib", lib)
+    for catch in catchers:
+        caught = False
+        try:
+            catch()
+        except (AssertionError, RuntimeError):
+            caught = True
+        assert caught, f"pin {catch.__name__} did not catch mutant {name}"
