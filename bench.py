@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of sparse MLA decode (SFA) + lse merge on GB300.
+
+One step = one full pass of the path over one batch of synthetic inputs:
+index resolution, latent-row gather, QK^T, online softmax, P.V, epilogue, and
+(for sharded workloads) the lse merge of the shard partials.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs the same
+workload on its own GPU (replicas: weak scaling, no data-path collective); the
+reported time is the max over ranks and `value` aggregates all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from deepseek_sparse_mla_sfa_gb300 import workloads  # noqa: E402
+
+METRIC = "sparse MLA decode TFLOP/s and gather GB/s (h=128, top_k=2048); % of roofline"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+ROW_BYTES = 576 * 2
+FLOPS_PER_ROW_HEAD = 2 * (576 + 512)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def accounting(inp: workloads.Inputs):
+    """Algorithmic work of one step: FLOPs and bytes per kernel (SURVEY-style accounting:
+    only the selected rows count; softmax exponentials are not FLOPs)."""
+    w = inp.w
+    T, h, n = w.T, w.h, w.n_splits
+    i = torch.arange(w.Q, device=inp.topk_idx.device).repeat(w.B)
+    L = inp.seq_lens.long().repeat_interleave(w.Q) - (w.Q - 1 - i)
+    idx = inp.topk_idx.long()
+    k_valid = ((idx >= 0) & (idx < L.unsqueeze(1))).sum(dim=1)
+    kv_total = int(k_valid.sum())
+    flops = FLOPS_PER_ROW_HEAD * h * kv_total
+    gather = kv_total * ROW_BYTES
+    q_b = T * h * 576 * 2
+    idx_b = T * w.top_k * 4
+    res_b = T * h * 513 * 4
+    decode_b = gather + q_b + idx_b + (res_b if n == 1 else n * res_b)
+    merge_b = n * res_b + res_b if n > 1 else 0
+    return {"k_valid_total": kv_total, "flops": flops, "gather_bytes": gather,
+            "decode_bytes": decode_b, "merge_bytes": merge_b, "total_bytes": decode_b + merge_b}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, t_begin, t_end):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [r.strip().split(",") for r in self.tmp.read().splitlines() if r.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_leg(inp, acc, target_s=15.0, max_tokens=None):
+    """Time the fp64 oracle, as it stands, on the host cores over a bounded sample of
+    the workload (whole tokens, all heads, all shards).  Returns (line dict, elapsed)."""
+    import numpy as np
+    import oracle
+    w = inp.w
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    prob = oracle.Problem(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.Q, w.scale)
+    L = (prob.seq_lens.repeat(w.Q) - (w.Q - 1 - np.tile(np.arange(w.Q), w.B))).astype(np.int64)
+    kval = ((prob.topk_idx >= 0) & (prob.topk_idx < L[:, None])).sum(axis=1)
+
+    def run(tokens):
+        t = np.repeat(tokens, w.h).astype(np.int32)
+        hh = np.tile(np.arange(w.h), len(tokens)).astype(np.int32)
+        t0 = time.perf_counter()
+        if w.n_splits > 1:
+            n = w.n_splits
+            r = np.tile(np.arange(n), len(t)).astype(np.int32)
+            op, lp = oracle.decode_sampled(prob, np.repeat(t, n), np.repeat(hh, n), shards=r,
+                                           n_splits=n, nthreads=cores)
+            oracle.merge(op.reshape(len(t), n, -1).transpose(1, 0, 2), lp.reshape(len(t), n).T)
+        else:
+            oracle.decode_sampled(prob, t, hh, nthreads=cores)
+        return time.perf_counter() - t0
+
+    t1 = run(np.array([0]))
+    n_tok = max(1, min(w.T, int(target_s / max(t1, 1e-6))))
+    if max_tokens:
+        n_tok = min(n_tok, max_tokens)
+    tokens = np.linspace(0, w.T - 1, n_tok).round().astype(np.int64)
+    tokens = np.unique(tokens)
+    el = run(tokens)
+    flops = FLOPS_PER_ROW_HEAD * w.h * int(kval[tokens].sum())
+    val = flops / el / 1e12
+    return {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(tokens)} of {w.T} query tokens of {w.name}, all {w.h} heads"
+                      f"{', all %d shards + merge' % w.n_splits if w.n_splits > 1 else ''}; "
+                      f"{el:.2f} s fp64 on {cores} host threads"}, el
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.CONFIGS[args.config]
+    inp = workloads.make(w, device="cuda")
+    acc = accounting(inp)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_leg(inp, acc, target_s=min(per_step, 5.0))
+    vals, tot = [], 0.0
+    line_cb = None
+    for _ in range(args.steps):
+        cb, el = cpu_oracle_leg(inp, acc, target_s=per_step)
+        vals.append(cb["value"])
+        tot += el
+        line_cb = cb
+    value = statistics.mean(vals) if vals else 0.0
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Q": w.Q, "h": w.h, "S": w.S,
+                       "top_k": w.top_k, "n_splits": w.n_splits},
+            "cpu_baseline": line_cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import deepseek_sparse_mla_sfa_gb300 as sfa
+    w = workloads.CONFIGS[args.config]
+    peaks = load_peaks()
+    inp = workloads.make(w, device="cuda")
+    acc = accounting(inp)
+    T, h, n = w.T, w.h, w.n_splits
+    dev = inp.q.device
+    out = torch.empty((T, h, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, h), dtype=torch.float32, device=dev)
+    op = torch.empty((n, T, h, 512), dtype=torch.float32, device=dev) if n > 1 else None
+    lp = torch.empty((n, T, h), dtype=torch.float32, device=dev) if n > 1 else None
+    wsb = sfa.workspace_bytes(w.B, w.Q, h, w.top_k, n)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_dec, tc_path = sfa.decode_launches(w.B, w.Q, h, w.top_k, w.block_size, n, merge=False)
+    launches_per_step = n_dec + (1 if n > 1 else 0)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record()
+        if n > 1:
+            sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                       n_splits=n, Q=w.Q, merge=False, out_part=op, lse_part=lp, workspace=ws)
+            if evs:
+                evs[1].record()
+            sfa.lse_merge(op, lp, out=out, lse=lse)
+        else:
+            sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                       n_splits=1, Q=w.Q, out=out, lse=lse, workspace=ws)
+            if evs:
+                evs[1].record()
+        if evs:
+            evs[2].record()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if sfa.last_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    for k in range(args.steps):
+        flush.zero_()                      # scrub L2 between timed steps (outside the events)
+        step(evs[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    t_end = time.time()
+    clk = clocks.stop(t_begin, t_end)
+    dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    mrg_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [a + b for a, b in zip(dec_ms, mrg_ms)]
+    local_ms = sum(step_ms) / max(1, len(step_ms))
+    ms = max_over_ranks(local_ms, world)
+    dec_avg = sum(dec_ms) / max(1, len(dec_ms))
+    mrg_avg = sum(mrg_ms) / max(1, len(mrg_ms))
+
+    value = world * acc["flops"] / (ms * 1e-3) / 1e12
+    gather_gbs = acc["gather_bytes"] / (ms * 1e-3) / 1e9
+    alg_gbs = acc["total_bytes"] / (ms * 1e-3) / 1e9
+    roof_s = max(acc["flops"] / (peaks["bf16_tflops"] * 1e12), acc["total_bytes"] / (peaks["hbm_gbs"] * 1e9))
+    dominant = "decode" if dec_avg >= mrg_avg else "lse_merge"
+    dom_ms = dec_avg if dominant == "decode" else mrg_avg
+    dom_bytes = acc["decode_bytes"] if dominant == "decode" else acc["merge_bytes"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = read_traffic(dominant, tc_path, w.name)
+
+    # end to end through the host-buffer entry point: H2D of the step's inputs, decode,
+    # D2H of out + lse, all inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(sfa, inp, args.steps, flush)
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        cpu, _ = cpu_oracle_leg(inp, acc, target_s=15.0)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Q": w.Q, "h": w.h, "S": w.S, "top_k": w.top_k,
+                   "n_splits": n, "block_size": w.block_size, "seed": w.seed,
+                   "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gather_gbs": gather_gbs, "algorithmic_gbs": alg_gbs,
+        "pct_of_roofline": 100.0 * roof_s / (ms * 1e-3),
+        "roofline_time_us": roof_s * 1e6,
+        "kernel_path": "tcgen05" if tc_path else "cuda-core",
+        "kernels": {"decode_ms": dec_avg, "lse_merge_ms": mrg_avg if n > 1 else None},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic, "peak_source": peaks["source"] + " (hbm copy)"},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def read_traffic(kernel: str, tc_path: bool, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this build."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    from deepseek_sparse_mla_sfa_gb300 import build as _b
+    src_hash = _b.source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#"):
+            k, wl, h, b = parts[:4]
+            if k == kernel and wl == workload and h == src_hash:
+                return float(b)
+    return None
+
+
+def run_e2e(sfa, inp, steps, flush):
+    w = inp.w
+    pin = lambda t: t.cpu().contiguous().pin_memory()
+    q_h, bt_h, sl_h, idx_h = pin(inp.q), pin(inp.block_table), pin(inp.seq_lens), pin(inp.topk_idx)
+    out_h = torch.empty((w.T, w.h, 512), dtype=torch.float32).pin_memory()
+    lse_h = torch.empty((w.T, w.h), dtype=torch.float32).pin_memory()
+    nbytes = sfa.decode_host_staging_bytes(w.B, w.Q, w.h, w.top_k, inp.max_blocks, w.n_splits)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device=inp.q.device)
+    call = lambda: sfa.decode_host(q_h, inp.kv, bt_h, sl_h, idx_h, w.scale, w.n_splits, w.Q,
+                                   out_h, lse_h, staging)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms = tot / max(1, steps)
+    acc = accounting(inp)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, bt_h, sl_h, idx_h))
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    return {"value": acc["flops"] / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "sfa_decode_host (pinned host buffers, device-resident cache)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=workloads.HEADLINE, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

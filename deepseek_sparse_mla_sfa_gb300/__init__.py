@@ -1,0 +1,190 @@
+"""GB300 (sm_103a) sparse MLA decode (SFA) with DCP-style split partials.
+
+A thin Python binding over the C ABI of libsfa.so (include/sfa.h).  It only
+checks and marshals arguments; every step of the computation runs in the
+library's CUDA kernels.  PyTorch provides device memory and streams.
+
+    out, lse = decode(q, kv, block_table, seq_lens, topk_idx, scale)
+    out_part, lse_part = decode(..., n_splits=8, merge=False)
+    out, lse = lse_merge(out_part, lse_part)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import SfaError
+
+D_QK = 576
+D_V = 512
+MAX_HEADS = 128
+MAX_SPLITS = 64
+
+__all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
+           "workspace_bytes", "decode_launches", "last_device_status", "set_wait_limit", "SfaError", "D_QK", "D_V"]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def workspace_bytes(B: int, Q: int, h: int, top_k: int, n_splits: int) -> int:
+    return int(_lib.load().sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits))
+
+
+def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int = 1, Q: int = 1,
+           merge: bool = True, out=None, lse=None, out_part=None, lse_part=None, workspace=None,
+           stream=None):
+    """Sparse MLA decode (C ABI ``sfa_decode``).
+
+    q [B*Q, h, 576] bf16, kv [num_blocks, block_size, 576] bf16, block_table [B, max_blocks]
+    int32, seq_lens [B] int32, topk_idx [B*Q, top_k] int32 (-1 = padding), all on one CUDA
+    device.  Returns (out [B*Q, h, 512] fp32, lse [B*Q, h] fp32); with n_splits > 1 and
+    merge=False returns the shard partials (out_part [n, B*Q, h, 512], lse_part [n, B*Q, h]).
+    """
+    lib = _lib.load()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode runs on a CUDA device only")
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _need(topk_idx, "topk_idx", torch.int32, dev, 2)
+    T, h, d = q.shape
+    if d != D_QK or kv.shape[2] != D_QK:
+        raise ValueError("q and kv rows must have 576 columns")
+    B = seq_lens.shape[0]
+    if T != B * Q or topk_idx.shape[0] != T or block_table.shape[0] != B:
+        raise ValueError("inconsistent B / Q / T")
+    top_k = topk_idx.shape[1]
+    num_blocks, block_size = kv.shape[0], kv.shape[1]
+    max_blocks = block_table.shape[1]
+    if n_splits == 1 or merge:
+        if out is None:
+            out = torch.empty((T, h, D_V), dtype=torch.float32, device=dev)
+        if lse is None:
+            lse = torch.empty((T, h), dtype=torch.float32, device=dev)
+        _need(out, "out", torch.float32, dev)
+        _need(lse, "lse", torch.float32, dev)
+    if n_splits > 1:
+        if out_part is None:
+            out_part = torch.empty((n_splits, T, h, D_V), dtype=torch.float32, device=dev)
+        if lse_part is None:
+            lse_part = torch.empty((n_splits, T, h), dtype=torch.float32, device=dev)
+        _need(out_part, "out_part", torch.float32, dev)
+        _need(lse_part, "lse_part", torch.float32, dev)
+    ws_need = int(lib.sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits))
+    if ws_need and workspace is None:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    code = lib.sfa_decode(_ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens), _ptr(topk_idx),
+                          B, Q, h, top_k, num_blocks, block_size, max_blocks, float(scale),
+                          n_splits, _ptr(out if (n_splits == 1 or merge) else None),
+                          _ptr(lse if (n_splits == 1 or merge) else None),
+                          _ptr(out_part if n_splits > 1 else None),
+                          _ptr(lse_part if n_splits > 1 else None), _ptr(workspace), ws_bytes,
+                          _stream_ptr(stream, dev))
+    _lib.check("sfa_decode", code)
+    if n_splits > 1 and not merge:
+        return out_part, lse_part
+    return out, lse
+
+
+def lse_merge(out_part, lse_part, out=None, lse=None, stream=None):
+    """Online-softmax merge over the leading axis (C ABI ``sfa_lse_merge``).
+
+    out_part [n, *rows, dv] fp32, lse_part [n, *rows] fp32 -> (out [*rows, dv], lse [*rows]).
+    """
+    lib = _lib.load()
+    dev = out_part.device
+    _need(out_part, "out_part", torch.float32, dev)
+    _need(lse_part, "lse_part", torch.float32, dev)
+    n = out_part.shape[0]
+    dv = out_part.shape[-1]
+    rows = lse_part[0].numel() if n > 0 else 0
+    if tuple(lse_part.shape) != tuple(out_part.shape[:-1]):
+        raise ValueError("lse_part must be out_part's shape without the last axis")
+    if out is None:
+        out = torch.empty(out_part.shape[1:], dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty(lse_part.shape[1:], dtype=torch.float32, device=dev)
+    code = lib.sfa_lse_merge(_ptr(out_part), _ptr(lse_part), n, rows, dv, _ptr(out), _ptr(lse),
+                             _stream_ptr(stream, dev))
+    _lib.check("sfa_lse_merge", code)
+    return out, lse
+
+
+def decode_host_staging_bytes(B, Q, h, top_k, max_blocks, n_splits) -> int:
+    return int(_lib.load().sfa_decode_host_staging_bytes(B, Q, h, top_k, max_blocks, n_splits))
+
+
+def decode_host(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, scale, n_splits,
+                Q, out_host, lse_host, staging, stream=None):
+    """One decode step with host-resident per-step inputs/outputs (C ABI ``sfa_decode_host``).
+
+    q/block_table/seq_lens/topk_idx and out/lse are (preferably pinned) CPU tensors, kv and
+    staging are on the device.  Enqueues copies + kernels on `stream`; synchronise before
+    reading out_host / lse_host.
+    """
+    lib = _lib.load()
+    dev = kv.device
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    for t, name, dt in ((q_host, "q_host", torch.bfloat16), (block_table_host, "block_table_host", torch.int32),
+                        (seq_lens_host, "seq_lens_host", torch.int32), (topk_idx_host, "topk_idx_host", torch.int32),
+                        (out_host, "out_host", torch.float32), (lse_host, "lse_host", torch.float32)):
+        _need(t, name, dt, torch.device("cpu"))
+    T, h, _ = q_host.shape
+    B = seq_lens_host.shape[0]
+    top_k = topk_idx_host.shape[1]
+    code = lib.sfa_decode_host(_ptr(q_host), _ptr(kv), _ptr(block_table_host), _ptr(seq_lens_host),
+                               _ptr(topk_idx_host), B, Q, h, top_k, kv.shape[0], kv.shape[1],
+                               block_table_host.shape[1], float(scale), n_splits, _ptr(out_host),
+                               _ptr(lse_host), _ptr(staging),
+                               staging.numel() * staging.element_size(), _stream_ptr(stream, dev))
+    _lib.check("sfa_decode_host", code)
+    return out_host, lse_host
+
+
+def decode_launches(B, Q, h, top_k, block_size, n_splits, merge=True):
+    """(kernels one decode call enqueues, whether the tcgen05 kernel serves it)."""
+    tc = ctypes.c_int(0)
+    n = int(_lib.load().sfa_decode_launches(B, Q, h, top_k, block_size, n_splits, int(bool(merge)),
+                                            ctypes.byref(tc)))
+    if n < 0:
+        raise ValueError("invalid decode shape")
+    return n, bool(tc.value)
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronise the stream, then return and clear the device status word (0 = OK)."""
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    return int(lib.sfa_last_device_status(_stream_ptr(stream, dev)))
+
+
+def set_wait_limit(iterations: int) -> int:
+    """Iteration cap of bounded device waits for later launches (0 = default)."""
+    return int(_lib.load().sfa_set_wait_limit(int(iterations)))

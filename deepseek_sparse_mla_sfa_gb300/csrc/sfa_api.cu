@@ -1,0 +1,266 @@
+// sfa_api.cu -- the C ABI of libsfa.so (declared in include/sfa.h): argument
+// checks, kernel selection, the per-device status word and the host-buffer
+// entry point.  Every step of the computation runs in this library's kernels.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/sfa.h"
+#include "sfa_internal.h"
+
+namespace {
+
+// Per-device status word written by kernels (first error wins), read and
+// cleared by sfa_last_device_status().
+__device__ int g_sfa_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+std::atomic<long long> g_wait_limit{0};
+constexpr long long kDefaultWaitLimit = 1LL << 26;  // iterations of a bounded device wait
+
+int* status_word(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_sfa_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+sfa_status check_decode_args(const void* q, const void* kv, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* topk_idx, int B, int Q, int h,
+                             int top_k, int num_blocks, int block_size, int max_blocks_per_seq,
+                             float scale, int n_splits) {
+  if (B < 0 || Q < 1 || top_k < 0 || num_blocks < 1 || block_size < 1 || max_blocks_per_seq < 1 ||
+      n_splits < 1 || h < 1 || !isfinite(scale))
+    return SFA_ERR_INVALID_ARG;
+  if (h > SFA_MAX_HEADS || n_splits > SFA_MAX_SPLITS) return SFA_ERR_UNSUPPORTED;
+  if ((long long)B * Q > 0x7fffffffLL) return SFA_ERR_UNSUPPORTED;
+  if ((long long)B * Q == 0) return SFA_OK;
+  if (!q || !kv || !block_table || !seq_lens || (!topk_idx && top_k > 0)) return SFA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(topk_idx, 4))
+    return SFA_ERR_INVALID_ARG;
+  return SFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sfa_status_string(sfa_status s) {
+  switch (s) {
+    case SFA_OK: return "SFA_OK";
+    case SFA_ERR_INVALID_ARG: return "SFA_ERR_INVALID_ARG";
+    case SFA_ERR_UNSUPPORTED: return "SFA_ERR_UNSUPPORTED";
+    case SFA_ERR_WORKSPACE: return "SFA_ERR_WORKSPACE";
+    case SFA_ERR_CUDA: return "SFA_ERR_CUDA";
+    case SFA_ERR_DEVICE_TIMEOUT: return "SFA_ERR_DEVICE_TIMEOUT";
+    case SFA_ERR_DEVICE_BAD_BLOCK: return "SFA_ERR_DEVICE_BAD_BLOCK";
+  }
+  return "SFA_UNKNOWN_STATUS";
+}
+
+long long sfa_set_wait_limit(long long iterations) {
+  return g_wait_limit.exchange(iterations < 0 ? 0 : iterations);
+}
+
+size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits) {
+  if (B <= 0 || Q <= 0 || h <= 0 || top_k < 0 || n_splits < 1) return 0;
+  return sfa::tc_workspace_bytes(B * Q, h, top_k, n_splits);
+}
+
+int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_splits, int merge,
+                        int* tensor_core_path) {
+  if (B < 0 || Q < 1 || h < 1 || h > SFA_MAX_HEADS || top_k < 0 || block_size < 1 ||
+      n_splits < 1 || n_splits > SFA_MAX_SPLITS)
+    return -1;
+  const bool tc = sfa::tc_supports(h, block_size);
+  if (tensor_core_path) *tensor_core_path = tc ? 1 : 0;
+  if ((long long)B * Q == 0) return 0;
+  int n = tc ? sfa::tc_launches(B * Q, h, top_k, n_splits) : 1;
+  if (n_splits > 1 && merge) n += 1;
+  return n;
+}
+
+sfa_status sfa_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,
+                         int dv, float* out, float* lse, sfa_stream stream) {
+  if (n_splits < 1 || rows < 0 || dv < 1) return SFA_ERR_INVALID_ARG;
+  if (n_splits > SFA_MAX_SPLITS) return SFA_ERR_UNSUPPORTED;
+  if (rows == 0) return SFA_OK;
+  if (!out_part || !lse_part || !out || !lse) return SFA_ERR_INVALID_ARG;
+  if (!aligned(out_part, 16) || !aligned(out, 16) || !aligned(lse_part, 4) || !aligned(lse, 4))
+    return SFA_ERR_INVALID_ARG;
+  cudaError_t e = sfa::launch_lse_merge(out_part, lse_part, n_splits, rows, dv, out, lse,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+sfa_status sfa_decode(const void* q, const void* kv, const int32_t* block_table,
+                      const int32_t* seq_lens, const int32_t* topk_idx, int B, int Q, int h,
+                      int top_k, int num_blocks, int block_size, int max_blocks_per_seq,
+                      float scale, int n_splits, float* out, float* lse, float* out_part,
+                      float* lse_part, void* workspace, size_t workspace_bytes,
+                      sfa_stream stream) {
+  sfa_status st = check_decode_args(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k,
+                                    num_blocks, block_size, max_blocks_per_seq, scale, n_splits);
+  if (st != SFA_OK) return st;
+  const int T = B * Q;
+  if (T == 0) return SFA_OK;
+  const bool merge_after = n_splits > 1 && out && lse;
+  if (n_splits == 1) {
+    if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return SFA_ERR_INVALID_ARG;
+  } else {
+    if (!out_part || !lse_part || !aligned(out_part, 16) || !aligned(lse_part, 4))
+      return SFA_ERR_INVALID_ARG;
+    if ((out && !lse) || (!out && lse)) return SFA_ERR_INVALID_ARG;
+    if (merge_after && (!aligned(out, 16) || !aligned(lse, 4))) return SFA_ERR_INVALID_ARG;
+  }
+  const size_t need = sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
+    return SFA_ERR_WORKSPACE;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
+  int* status = status_word(dev);
+  if (!status) return SFA_ERR_CUDA;
+
+  sfa::DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.topk_idx = topk_idx;
+  p.B = B;
+  p.Q = Q;
+  p.h = h;
+  p.top_k = top_k;
+  p.num_blocks = num_blocks;
+  p.block_size = block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.scale = scale;
+  p.n_splits = n_splits;
+  p.out = n_splits == 1 ? out : out_part;
+  p.lse = n_splits == 1 ? lse : lse_part;
+  p.workspace = workspace;
+  p.workspace_bytes = workspace_bytes;
+  p.status = status;
+  const long long wl = g_wait_limit.load();
+  p.wait_limit = wl > 0 ? wl : kDefaultWaitLimit;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = sfa::tc_supports(h, block_size) ? sfa::launch_decode_tc(p, s)
+                                                  : sfa::launch_decode_simt(p, s);
+  if (e != cudaSuccess) return SFA_ERR_CUDA;
+  if (merge_after) {
+    e = sfa::launch_lse_merge(out_part, lse_part, n_splits, T * h, SFA_D_V, out, lse, s);
+    if (e != cudaSuccess) return SFA_ERR_CUDA;
+  }
+  return SFA_OK;
+}
+
+size_t sfa_decode_host_staging_bytes(int B, int Q, int h, int top_k, int max_blocks_per_seq,
+                                     int n_splits) {
+  if (B < 0 || Q < 1 || h < 1 || top_k < 0 || max_blocks_per_seq < 1 || n_splits < 1) return 0;
+  const size_t T = (size_t)B * Q, a = 256;
+  size_t n = 0;
+  n += round_up(T * h * SFA_D_QK * 2, a);                 // q
+  n += round_up((size_t)B * max_blocks_per_seq * 4, a);   // block_table
+  n += round_up((size_t)B * 4, a);                        // seq_lens
+  n += round_up(T * top_k * 4, a);                        // topk_idx
+  n += round_up(T * h * SFA_D_V * 4, a);                  // out
+  n += round_up(T * h * 4, a);                            // lse
+  if (n_splits > 1) {
+    n += round_up((size_t)n_splits * T * h * SFA_D_V * 4, a);  // out_part
+    n += round_up((size_t)n_splits * T * h * 4, a);            // lse_part
+  }
+  n += round_up(sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits), a);
+  return n;
+}
+
+sfa_status sfa_decode_host(const void* q_host, const void* kv, const int32_t* block_table_host,
+                           const int32_t* seq_lens_host, const int32_t* topk_idx_host, int B,
+                           int Q, int h, int top_k, int num_blocks, int block_size,
+                           int max_blocks_per_seq, float scale, int n_splits, float* out_host,
+                           float* lse_host, void* staging, size_t staging_bytes,
+                           sfa_stream stream) {
+  sfa_status st = check_decode_args(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, B,
+                                    Q, h, top_k, num_blocks, block_size, max_blocks_per_seq, scale,
+                                    n_splits);
+  if (st != SFA_OK) return st;
+  const size_t T = (size_t)B * Q;
+  if (T == 0) return SFA_OK;
+  if (!out_host || !lse_host) return SFA_ERR_INVALID_ARG;
+  const size_t need = sfa_decode_host_staging_bytes(B, Q, h, top_k, max_blocks_per_seq, n_splits);
+  if (!staging || staging_bytes < need || !aligned(staging, 256)) return SFA_ERR_WORKSPACE;
+
+  char* base = static_cast<char*>(staging);
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    char* p = base + off;
+    off += round_up(bytes, 256);
+    return p;
+  };
+  const size_t q_bytes = T * h * SFA_D_QK * 2, bt_bytes = (size_t)B * max_blocks_per_seq * 4,
+               sl_bytes = (size_t)B * 4, idx_bytes = T * top_k * 4,
+               out_bytes = T * h * SFA_D_V * 4, lse_bytes = T * h * 4;
+  void* q_d = carve(q_bytes);
+  int32_t* bt_d = reinterpret_cast<int32_t*>(carve(bt_bytes));
+  int32_t* sl_d = reinterpret_cast<int32_t*>(carve(sl_bytes));
+  int32_t* idx_d = reinterpret_cast<int32_t*>(carve(idx_bytes));
+  float* out_d = reinterpret_cast<float*>(carve(out_bytes));
+  float* lse_d = reinterpret_cast<float*>(carve(lse_bytes));
+  float* op_d = nullptr;
+  float* lp_d = nullptr;
+  if (n_splits > 1) {
+    op_d = reinterpret_cast<float*>(carve((size_t)n_splits * out_bytes));
+    lp_d = reinterpret_cast<float*>(carve((size_t)n_splits * lse_bytes));
+  }
+  const size_t ws_bytes = sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits);
+  void* ws_d = ws_bytes ? carve(ws_bytes) : nullptr;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(q_d, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(bt_d, block_table_host, bt_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(sl_d, seq_lens_host, sl_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      (idx_bytes && cudaMemcpyAsync(idx_d, topk_idx_host, idx_bytes, cudaMemcpyHostToDevice, s) !=
+                        cudaSuccess))
+    return SFA_ERR_CUDA;
+  st = sfa_decode(q_d, kv, bt_d, sl_d, idx_d, B, Q, h, top_k, num_blocks, block_size,
+                  max_blocks_per_seq, scale, n_splits, out_d, lse_d, op_d, lp_d, ws_d, ws_bytes,
+                  stream);
+  if (st != SFA_OK) return st;
+  if (cudaMemcpyAsync(out_host, out_d, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse_host, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SFA_ERR_CUDA;
+  return SFA_OK;
+}
+
+sfa_status sfa_last_device_status(sfa_stream stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
+  int* status = status_word(dev);
+  if (!status) return SFA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SFA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SFA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return SFA_ERR_CUDA;
+  return static_cast<sfa_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// sfa_internal.h -- declarations shared by the translation units of libsfa.so.
+// Not part of the public ABI (that is include/sfa.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sfa {
+
+constexpr int kDQK = 576;  // kv_lora_rank + qk_rope_head_dim
+constexpr int kDV = 512;   // kv_lora_rank
+constexpr int kMaxHeads = 128;
+constexpr int kMaxSplits = 64;
+
+// Device status codes (mirror sfa_status values).
+constexpr int kStatusTimeout = -5;
+constexpr int kStatusBadBlock = -6;
+
+// One decode problem as the kernels see it.  Pointers are device pointers.
+struct DecodeParams {
+  const __nv_bfloat16* q;    // [T, h, 576]
+  const __nv_bfloat16* kv;   // [num_blocks, block_size, 576]
+  const int32_t* block_table;  // [B, max_blocks]
+  const int32_t* seq_lens;     // [B]
+  const int32_t* topk_idx;     // [T, top_k]
+  int B, Q, h, top_k, num_blocks, block_size, max_blocks;
+  float scale;
+  int n_splits;
+  float* out;  // n_splits == 1: [T, h, 512]; else partials [n_splits, T, h, 512]
+  float* lse;  // n_splits == 1: [T, h];      else partials [n_splits, T, h]
+  void* workspace;
+  size_t workspace_bytes;
+  int* status;            // per-device status word
+  long long wait_limit;   // iteration cap of every bounded device wait
+};
+
+// Record the first device-side error in the status word (never traps).
+__device__ __forceinline__ void report_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Shard bounds of sequence `seq_len` for shard r of n (n == 1: the whole cache),
+// intersected with the causal range [0, L).
+__host__ __device__ __forceinline__ void shard_bounds(int seq_len, int L, int r, int n, int& lo,
+                                                      int& hi) {
+  if (n <= 1) {
+    lo = 0;
+    hi = L;
+    return;
+  }
+  int c = seq_len > 0 ? (seq_len + n - 1) / n : 0;
+  long long l = (long long)r * c, u = (long long)(r + 1) * c;
+  if (u > L) u = L;
+  lo = (int)(l > 0x7fffffff ? 0x7fffffff : l);
+  hi = (int)(u < lo ? lo : u);
+}
+
+// Launchers (return the launch error, if any).
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,
+                             int dv, float* out, float* lse, cudaStream_t stream);
+
+// tcgen05 path: whether it handles this problem, its workspace, and its launch.
+bool tc_supports(int h, int block_size);
+size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits);
+int tc_launches(int T, int h, int top_k, int n_splits);
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace sfa

@@ -1,0 +1,187 @@
+/*
+ * sfa.h -- C ABI of the GB300 (sm_103a) sparse MLA decode library (libsfa.so).
+ *
+ * One decode step of DeepSeek-style sparse attention (SFA) over a paged MLA
+ * latent KV cache, plus the online-softmax merge of per-shard (out, lse)
+ * partials used by decode context parallelism (DCP).
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" must point to memory of the current CUDA device;
+ *    pointers marked "host" to host memory (pinned memory gives asynchronous
+ *    copies).  The caller allocates and owns every buffer; the library never
+ *    allocates, frees or keeps a pointer after a call returns.
+ *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
+ *    default stream).  Calls only enqueue work on it and return without
+ *    synchronising, except sfa_last_device_status() and the host-buffer entry
+ *    point's error path, which say so.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns an error code and launches nothing.  Problems only the
+ *    device can see (a block-table entry outside [0, num_blocks) for a selected
+ *    position, a bounded wait that ran out) are recorded in a per-device status
+ *    word read by sfa_last_device_status().  The offending row is skipped,
+ *    never dereferenced.
+ *  - Layouts are dense, row-major, with no padding between rows.
+ */
+#ifndef SFA_H
+#define SFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SFA_OK = 0,
+  SFA_ERR_INVALID_ARG = -1,    /* null pointer, negative size, misaligned buffer, bad value   */
+  SFA_ERR_UNSUPPORTED = -2,    /* valid but outside what the kernels implement (e.g. h > 128)  */
+  SFA_ERR_WORKSPACE = -3,      /* workspace / staging buffer missing or too small              */
+  SFA_ERR_CUDA = -4,           /* a CUDA runtime call failed (launch error, copy error)        */
+  SFA_ERR_DEVICE_TIMEOUT = -5, /* a bounded device-side wait gave up (device status only)      */
+  SFA_ERR_DEVICE_BAD_BLOCK = -6 /* a selected position mapped to an invalid block (device)     */
+} sfa_status;
+
+typedef void *sfa_stream; /* a cudaStream_t */
+
+#define SFA_D_QK 576     /* kv_lora_rank (512) + qk_rope_head_dim (64) */
+#define SFA_D_V 512      /* kv_lora_rank: V is the latent part of the row */
+#define SFA_MAX_HEADS 128
+#define SFA_MAX_SPLITS 64
+
+/*
+ * sfa_decode -- sparse attention of each query token over its selected latent
+ * cache rows.
+ *
+ * Defined by: "RFC: MsModeling 支持 Decode Context Parallel 仿真" 2.1.4.1 (paged MLA
+ * latent cache [N_blk, block_size, kv_lora_rank + qk_rope_head_dim] and block
+ * table), 2.1.4.2 / 2.1.4.4 (attention output plus fp32 lse [B*Q, heads]), 1.1 and
+ * 2.1.1 (KV sharded along the sequence, partial (out, lse) per shard);
+ * "vllm-ascend PR #18870 解读" 4.3 / 4.5 (fused QK^T -> softmax -> .V over the
+ * top-2048 selected entries, latent shared by all heads); "RFC: Context Parallel
+ * Modeling for DeepSeek-Style Attention" 3.6 (bf16 SFA inputs).
+ *
+ * For query token t = b*Q + i (0 <= i < Q) and head hh:
+ *   L_t   = seq_lens[b] - (Q - 1 - i)              (token i sees one more position than i-1)
+ *   entry j is used iff 0 <= topk_idx[t, j] < L_t   (anything else, e.g. -1, is padding)
+ *   row   = block_table[b, p / block_size] * block_size + p % block_size
+ *   s_j   = scale * dot(q[t, hh, 0:576], kv[row, 0:576])
+ *   out   = softmax(s) . kv[rows, 0:512],   lse = ln sum_j exp(s_j)   (natural log)
+ *   no entry used -> out = 0, lse = -inf
+ * Duplicate entries count once per list entry.
+ *
+ * Shards (n_splits > 1, decode context parallelism on one GPU): shard r covers
+ * positions [r*c, (r+1)*c) of sequence b with c = ceil(seq_lens[b] / n_splits),
+ * intersected with the token's causal range; each shard is attended on its own
+ * into out_part[r], lse_part[r] (empty shard -> 0, -inf).
+ *
+ * Arguments:
+ *   q           device, bf16 [B*Q, h, 576]
+ *   kv          device, bf16 [num_blocks, block_size, 576]; V = columns 0..511
+ *   block_table device, int32 [B, max_blocks_per_seq]; entries for blocks a sequence
+ *               does not own are never read (any value)
+ *   seq_lens    device, int32 [B]: cache length of each sequence (includes the Q new tokens)
+ *   topk_idx    device, int32 [B*Q, top_k]: logical positions, -1 = padding
+ *   B >= 0, Q >= 1, 1 <= h <= 128, top_k >= 0, num_blocks >= 1, block_size >= 1,
+ *   max_blocks_per_seq >= 1, scale finite, 1 <= n_splits <= 64
+ *   out, lse    device, fp32 [B*Q, h, 512] and [B*Q, h]: the final result.  Required
+ *               when n_splits == 1.  When n_splits > 1 they may be NULL (only the
+ *               partials are produced); if given, the partials are also merged
+ *               into them on the same stream (as sfa_lse_merge does).
+ *   out_part, lse_part  device, fp32 [n_splits, B*Q, h, 512] and [n_splits, B*Q, h];
+ *               required when n_splits > 1, ignored otherwise.
+ *   workspace   device scratch of at least sfa_decode_workspace_bytes(...) bytes,
+ *               256-byte aligned (may be NULL when that size is 0).  Its contents
+ *               need no initialisation and are undefined afterwards.
+ *   All float/bf16 buffers must be 16-byte aligned.
+ * Returns SFA_OK, or an error code with nothing launched.
+ */
+sfa_status sfa_decode(const void *q, const void *kv, const int32_t *block_table,
+                      const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h,
+                      int top_k, int num_blocks, int block_size, int max_blocks_per_seq,
+                      float scale, int n_splits, float *out, float *lse, float *out_part,
+                      float *lse_part, void *workspace, size_t workspace_bytes,
+                      sfa_stream stream);
+
+/*
+ * sfa_decode_workspace_bytes -- device scratch sfa_decode needs for this shape
+ * (internal split of long selections into chunks, merged on the device).  May be 0.
+ */
+size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits);
+
+/*
+ * sfa_lse_merge -- online-softmax merge of n_splits partial results.
+ *
+ * Defined by: "RFC: MsModeling 支持 Decode Context Parallel 仿真" 1.1 and 2.1.1 (the
+ * local online-softmax merge after the all-to-all of output and lse) and 2.1.4.3
+ * (both exchanged in fp32).  For each row x:
+ *   M = max_r lse_part[r, x];  lse[x] = M + ln sum_r exp(lse_part[r, x] - M)
+ *   out[x, :] = sum_r exp(lse_part[r, x] - lse[x]) * out_part[r, x, :]
+ *   every lse_part[r, x] = -inf  ->  out[x, :] = 0, lse[x] = -inf
+ *
+ *   out_part device fp32 [n_splits, rows, dv], lse_part device fp32 [n_splits, rows]
+ *   out      device fp32 [rows, dv],           lse      device fp32 [rows]
+ *   1 <= n_splits <= 64, rows >= 0, dv >= 1; float buffers 16-byte aligned.
+ *   out/lse must not overlap out_part/lse_part.
+ */
+sfa_status sfa_lse_merge(const float *out_part, const float *lse_part, int n_splits, int rows,
+                         int dv, float *out, float *lse, sfa_stream stream);
+
+/*
+ * sfa_decode_host -- one decode step whose per-step inputs and outputs live in
+ * host memory, with the latent cache resident on the device (the form a serving
+ * loop that keeps its cache in HBM uses).  Enqueues on `stream`: host->device
+ * copies of q, block_table, seq_lens and topk_idx into `staging`, sfa_decode,
+ * and device->host copies of out and lse.  The caller synchronises the stream
+ * before reading out_host / lse_host.
+ *
+ *   q_host, block_table_host, seq_lens_host, topk_idx_host: host, layouts as in sfa_decode
+ *   kv           device, as in sfa_decode
+ *   out_host, lse_host: host fp32 [B*Q, h, 512] and [B*Q, h] (the merged result)
+ *   staging      device scratch of at least sfa_decode_host_staging_bytes(...) bytes,
+ *                256-byte aligned; holds the device copies, partials and workspace.
+ * Host buffers must stay valid until the stream reaches the end of the copies.
+ */
+size_t sfa_decode_host_staging_bytes(int B, int Q, int h, int top_k, int max_blocks_per_seq,
+                                     int n_splits);
+sfa_status sfa_decode_host(const void *q_host, const void *kv, const int32_t *block_table_host,
+                           const int32_t *seq_lens_host, const int32_t *topk_idx_host, int B,
+                           int Q, int h, int top_k, int num_blocks, int block_size,
+                           int max_blocks_per_seq, float scale, int n_splits, float *out_host,
+                           float *lse_host, void *staging, size_t staging_bytes,
+                           sfa_stream stream);
+
+/*
+ * sfa_last_device_status -- synchronises `stream`, then returns and clears the
+ * current device's status word: SFA_OK, SFA_ERR_DEVICE_TIMEOUT (a bounded wait
+ * inside a kernel gave up; that kernel's outputs are undefined) or
+ * SFA_ERR_DEVICE_BAD_BLOCK (a selected position's block-table entry was outside
+ * [0, num_blocks); that row was skipped).  SFA_ERR_CUDA if the stream itself failed.
+ */
+sfa_status sfa_last_device_status(sfa_stream stream);
+
+/*
+ * sfa_decode_launches -- how many kernels one sfa_decode call with these
+ * arguments enqueues (merge != 0: out/lse given with n_splits > 1), and through
+ * *tensor_core_path whether the tcgen05 kernel serves it (1) or the CUDA-core
+ * kernel (0).  tensor_core_path may be NULL.  Returns -1 for invalid arguments.
+ */
+int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_splits, int merge,
+                        int *tensor_core_path);
+
+/* sfa_status_string -- static, human-readable name of a status code. */
+const char *sfa_status_string(sfa_status s);
+
+/*
+ * sfa_set_wait_limit -- test hook for the failure path: sets the iteration cap
+ * of every bounded device-side wait in kernels launched afterwards from this
+ * process (0 restores the default).  With a tiny cap a wait gives up early and
+ * the kernel reports SFA_ERR_DEVICE_TIMEOUT through sfa_last_device_status()
+ * instead of hanging.  Returns the previous cap.
+ */
+long long sfa_set_wait_limit(long long iterations);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SFA_H */

@@ -1,0 +1,83 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports every
+function include/sfa.h declares, and its host-side argument checks return the
+documented codes before touching the GPU."""
+import ctypes
+
+import pytest
+
+from deepseek_sparse_mla_sfa_gb300 import _lib, build
+
+P0 = ctypes.c_void_p(0)
+FAKE = ctypes.c_void_p(1 << 20)   # a non-null, 256-aligned address; never dereferenced here
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_header_functions_are_all_exported(lib):
+    names = _lib.header_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/sfa.h but not exported"
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature in the binding"
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.sfa_status_string(code).decode() == name
+    assert lib.sfa_status_string(12345).decode() == "SFA_UNKNOWN_STATUS"
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, idx=FAKE, B=2, Q=1, h=4, top_k=8, nb=4, bs=64,
+             mb=4, scale=0.07, n=1, out=FAKE, lse=FAKE, op=P0, lp=P0, ws=P0, wsb=0, stream=P0)
+    a.update(kw)
+    return lib.sfa_decode(a["q"], a["kv"], a["bt"], a["sl"], a["idx"], a["B"], a["Q"], a["h"],
+                          a["top_k"], a["nb"], a["bs"], a["mb"], a["scale"], a["n"], a["out"],
+                          a["lse"], a["op"], a["lp"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=P0), -1), (dict(kv=P0), -1), (dict(idx=P0), -1), (dict(out=P0), -1),
+    (dict(h=0), -1), (dict(h=129), -2), (dict(Q=0), -1), (dict(B=-1), -1), (dict(n=0), -1),
+    (dict(n=65), -2), (dict(bs=0), -1), (dict(nb=0), -1), (dict(mb=0), -1),
+    (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
+    (dict(q=ctypes.c_void_p((1 << 20) + 8)), -1),           # q not 16-byte aligned
+    (dict(n=2), -1),                                        # partial buffers missing
+    (dict(n=2, op=FAKE, lp=FAKE, out=FAKE, lse=P0), -1),     # out without lse
+    (dict(B=0), 0), (dict(B=0, q=P0, kv=P0), 0),             # nothing to do
+])
+def test_host_argument_checks(lib, kw, code):
+    assert _decode(lib, **kw) == code
+
+
+def test_merge_argument_checks(lib):
+    m = lib.sfa_lse_merge
+    assert m(FAKE, FAKE, 0, 4, 512, FAKE, FAKE, P0) == -1
+    assert m(FAKE, FAKE, 65, 4, 512, FAKE, FAKE, P0) == -2
+    assert m(FAKE, FAKE, 2, -1, 512, FAKE, FAKE, P0) == -1
+    assert m(FAKE, FAKE, 2, 4, 0, FAKE, FAKE, P0) == -1
+    assert m(P0, FAKE, 2, 4, 512, FAKE, FAKE, P0) == -1
+    assert m(FAKE, FAKE, 2, 0, 512, P0, P0, P0) == 0       # zero rows: nothing to do
+
+
+def test_workspace_and_staging_sizes(lib):
+    assert lib.sfa_decode_workspace_bytes(0, 1, 4, 8, 1) == 0
+    ws = lib.sfa_decode_workspace_bytes(64, 1, 128, 2048, 1)
+    assert ws % 256 == 0
+    st1 = lib.sfa_decode_host_staging_bytes(64, 1, 128, 2048, 512, 1)
+    st8 = lib.sfa_decode_host_staging_bytes(64, 1, 128, 2048, 512, 8)
+    need = 64 * 128 * 576 * 2 + 64 * 512 * 4 + 64 * 4 + 64 * 2048 * 4 + 64 * 128 * 513 * 4
+    assert st1 >= need and st8 >= st1 + 8 * 64 * 128 * 513 * 4
+    # a staging buffer that is too small is refused before any copy
+    small = lib.sfa_decode_host(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 1, 4, 8, 4, 64, 4, 0.07, 1, FAKE,
+                                FAKE, FAKE, 16, P0)
+    assert small == -3
+
+
+def test_wait_limit_hook_roundtrip(lib):
+    old = lib.sfa_set_wait_limit(123)
+    assert lib.sfa_set_wait_limit(old) == 123

@@ -1,0 +1,225 @@
+"""GPU parity of sfa_decode / sfa_lse_merge (through the C ABI) against the fp64
+oracle on the same seeded inputs.
+
+* small and mid-size cases: every output element, every shard partial;
+* the five workloads at full size, in the launch configuration the benchmark
+  times: sampled (token, head) outputs the oracle computes one by one, plus
+  properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import deepseek_sparse_mla_sfa_gb300 as sfa
+import oracle
+from deepseek_sparse_mla_sfa_gb300 import workloads
+from tests.gpu_helpers import compare, problem_of, run_cuda, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.Workload
+
+# element-by-element cases: several tiles of the kernels, ragged tails, odd head counts
+SMALL = [
+    workloads.CONFIGS["tiny"],
+    workloads.small("tiny", n_splits=1),
+    W("h128_ragged", B=3, Q=1, h=128, S=2048, top_k=333, n_splits=1, index_kind="uniform", seed=7),
+    W("h128_k2048", B=2, Q=1, h=128, S=8192, top_k=2048, n_splits=1, index_kind="uniform", seed=8),
+    W("h64_mtp", B=3, Q=2, h=64, S=3000, S_min=100, top_k=700, n_splits=1, index_kind="causal", seed=9),
+    W("h16_dense_splits", B=2, Q=1, h=16, S=1000, top_k=1000, n_splits=4, index_kind="dense", seed=10),
+    W("h128_dcp", B=2, Q=1, h=128, S=20000, recent=2000, top_k=512, n_splits=8,
+      index_kind="dcp_long", seed=11),
+    W("h1", B=2, Q=1, h=1, S=500, top_k=129, n_splits=1, index_kind="uniform", seed=12),
+    W("h3_bs16", B=2, Q=1, h=3, S=700, top_k=200, n_splits=3, index_kind="uniform", block_size=16, seed=13),
+    W("h33_bs1", B=1, Q=1, h=33, S=300, top_k=150, n_splits=1, index_kind="uniform", block_size=1, seed=14),
+    W("h100_q3", B=2, Q=3, h=100, S=900, S_min=1, top_k=257, n_splits=2, index_kind="causal", seed=15),
+    W("h65_spare", B=2, Q=1, h=65, S=640, top_k=640, n_splits=1, index_kind="uniform", spare_blocks=5, seed=16),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_cases_every_element(w):
+    inp = workloads.make(w, device="cuda")
+    prob = problem_of(inp)
+    ref_out, ref_lse = oracle.decode(prob)
+    out, lse = run_cuda(inp)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_out, ref_lse, w.name)
+    if w.n_splits > 1:
+        op, lp = run_cuda(inp, merge=False)
+        rop, rlp = oracle.decode_splits(prob, w.n_splits)
+        compare(op, lp, rop, rlp, w.name + " partials")
+        # the merge kernel on the partials alone
+        mo, ml = sfa.lse_merge(op, lp)
+        compare(mo, ml, ref_out, ref_lse, w.name + " lse_merge")
+    assert sfa.last_device_status() == 0
+
+
+FULL = ["tiny", "dense", "sfa_h128", "mtp", "long_dcp"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w = workloads.CONFIGS[name]
+    inp = workloads.make(w, device="cuda")
+    out, lse = run_cuda(inp)          # the launch configuration the benchmark times
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    prob = problem_of(inp)
+    t, hh = sample_pairs(w.T, w.h, 40, seed=sum(map(ord, name)))
+    ro, rl = oracle.decode_sampled(prob, t, hh)
+    compare(out[t, hh], lse[t, hh], ro, rl, name + " sampled")
+    if w.n_splits > 1:
+        op, lp = run_cuda(inp, merge=False)
+        r = np.random.default_rng(1).integers(0, w.n_splits, len(t)).astype(np.int32)
+        rop, rlp = oracle.decode_sampled(prob, t, hh, shards=r, n_splits=w.n_splits)
+        compare(op[r, t, hh], lp[r, t, hh], rop, rlp, name + " sampled partials")
+        # property at full size: merged shards == one unsplit pass
+        uo, ul = run_cuda(inp, n_splits=1)
+        e = (uo - out).abs().max().item()
+        el = (ul - lse).abs().max().item()
+        assert e < 2e-2 and el < 1e-3, (e, el)
+    assert sfa.last_device_status() == 0
+
+
+# ------------------------------------------------------------------------------------------
+# edge cases and exact index handling
+# ------------------------------------------------------------------------------------------
+def _inputs(w, **mods):
+    inp = workloads.make(w, device="cuda")
+    for k, v in mods.items():
+        setattr(inp, k, v)
+    return inp
+
+
+def test_empty_rows_and_zero_top_k():
+    w = W("edge", B=3, Q=1, h=8, S=300, top_k=40, n_splits=2, index_kind="uniform", seed=21)
+    inp = workloads.make(w, device="cuda")
+    inp.topk_idx[1] = -1                       # token 1: nothing selected
+    inp.topk_idx[2, :20] = 10 ** 6            # token 2: half out of range
+    prob = problem_of(inp)
+    ro, rl = oracle.decode(prob)
+    out, lse = run_cuda(inp)
+    compare(out, lse, ro, rl, "empty rows")
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    # top_k = 0
+    inp0 = workloads.make(w, device="cuda")
+    inp0.topk_idx = torch.empty((w.T, 0), dtype=torch.int32, device="cuda")
+    out0, lse0 = run_cuda(inp0)
+    assert torch.all(out0 == 0) and torch.all(torch.isneginf(lse0))
+
+
+def test_zero_tokens_is_a_no_op():
+    w = W("zero", B=0, Q=1, h=8, S=64, top_k=4, n_splits=1, index_kind="uniform", seed=22)
+    q = torch.empty((0, 8, 576), dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros((1, 64, 576), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((0, 1), dtype=torch.int32, device="cuda")
+    sl = torch.zeros((0,), dtype=torch.int32, device="cuda")
+    idx = torch.zeros((0, 4), dtype=torch.int32, device="cuda")
+    out, lse = sfa.decode(q, kv, bt, sl, idx, w.scale)
+    assert out.shape == (0, 8, 512) and lse.shape == (0, 8)
+
+
+def test_short_and_empty_sequences_with_mtp():
+    # seq_len 0 and seq_len < Q-1: every entry of those tokens is outside the causal range
+    w = W("short", B=3, Q=3, h=4, S=200, S_min=1, top_k=30, n_splits=1, index_kind="causal", seed=23)
+    inp = workloads.make(w, device="cuda")
+    inp.seq_lens[0] = 0
+    inp.seq_lens[1] = 1
+    inp.topk_idx[:6] = torch.arange(30, device="cuda", dtype=torch.int32) - 3
+    prob = problem_of(inp)
+    ro, rl = oracle.decode(prob)
+    out, lse = run_cuda(inp)
+    compare(out, lse, ro, rl, "short sequences")
+
+
+def test_unreferenced_rows_poisoned_with_nan():
+    # every cache row that no valid entry references is NaN: a stray read poisons the output
+    w = W("poison", B=2, Q=1, h=128, S=4096, top_k=600, n_splits=2, index_kind="uniform",
+          spare_blocks=4, seed=24)
+    inp = workloads.make(w, device="cuda")
+    inp.topk_idx[:, ::7] = -1
+    inp.topk_idx[:, 1::11] = 5000 + torch.arange(inp.topk_idx[:, 1::11].shape[1], device="cuda",
+                                                 dtype=torch.int32)
+    ref_out, ref_lse = oracle.decode(problem_of(inp))
+    keep = torch.zeros(inp.kv.shape[0] * inp.kv.shape[1], dtype=torch.bool, device="cuda")
+    bs = w.block_size
+    for b in range(w.B):
+        p = inp.topk_idx[b]
+        p = p[(p >= 0) & (p < inp.seq_lens[b])].long()
+        keep[inp.block_table[b, p // bs].long() * bs + p % bs] = True
+    flat = inp.kv.view(-1, 576)
+    flat[~keep] = float("nan")
+    out, lse = run_cuda(inp)
+    compare(out, lse, ref_out, ref_lse, "NaN-poisoned cache")
+    op, lp = run_cuda(inp, merge=False)
+    assert torch.isfinite(op).all()
+
+
+def test_one_hot_rows_recover_the_rows_read_exactly():
+    # q = 0 and the latent row of position p is one-hot at column p % 512 with distinct
+    # residues, so round(out * k_valid) is the exact set of rows the kernel read.
+    w = W("onehot", B=2, Q=1, h=128, S=4096, top_k=512, n_splits=1, index_kind="uniform", seed=25)
+    inp = workloads.make(w, device="cuda")
+    inp.q.zero_()
+    bs = w.block_size
+    expected = torch.zeros((w.B, 512), device="cuda")
+    for b in range(w.B):
+        pos = torch.randperm(512, device="cuda")[:300] + 512 * torch.randint(0, 8, (300,), device="cuda")
+        inp.topk_idx[b] = -1
+        inp.topk_idx[b, :300] = pos.to(torch.int32)
+        rows = inp.block_table[b, pos // bs].long() * bs + pos % bs
+        flat = inp.kv.view(-1, 576)
+        flat[rows] = 0
+        flat[rows, pos % 512] = 1
+        expected[b, pos % 512] = 1
+    out, lse = run_cuda(inp)
+    for b in range(w.B):
+        for hh in (0, 63, 64, 127):
+            got = torch.round(out[b, hh] * 300)
+            assert torch.equal(got, expected[b]), f"token {b} head {hh}"
+    assert torch.allclose(lse, torch.full_like(lse, float(np.log(300))), atol=1e-5)
+
+
+def test_duplicate_entries_count_per_entry():
+    w = W("dup", B=2, Q=1, h=128, S=1024, top_k=300, n_splits=1, index_kind="uniform", seed=26)
+    inp = workloads.make(w, device="cuda")
+    inp.topk_idx[:, 150:] = inp.topk_idx[:, :150]
+    ro, rl = oracle.decode(problem_of(inp))
+    out, lse = run_cuda(inp)
+    compare(out, lse, ro, rl, "duplicates")
+
+
+def test_bad_block_table_entry_is_reported_not_read():
+    w = W("badblk", B=2, Q=1, h=16, S=512, top_k=64, n_splits=1, index_kind="uniform", seed=27)
+    inp = workloads.make(w, device="cuda")
+    sfa.last_device_status()
+    inp.block_table[0, :] = inp.kv.shape[0] + 1000     # every block of sequence 0 is invalid
+    out, lse = run_cuda(inp)
+    assert sfa.last_device_status() == -6
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert sfa.last_device_status() == 0                # the status word was cleared
+
+
+def test_invalid_arguments_raise():
+    w = workloads.CONFIGS["tiny"]
+    inp = workloads.make(w, device="cuda")
+    with pytest.raises(sfa.SfaError):
+        sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, float("nan"))
+    with pytest.raises(TypeError):
+        sfa.decode(inp.q.float(), inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, 0.1)
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    w = W("host", B=4, Q=2, h=64, S=3000, S_min=200, top_k=500, n_splits=2, index_kind="causal", seed=28)
+    inp = workloads.make(w, device="cuda")
+    out, lse = run_cuda(inp)
+    pin = lambda t: t.cpu().pin_memory()
+    out_h = torch.empty((w.T, w.h, 512), dtype=torch.float32).pin_memory()
+    lse_h = torch.empty((w.T, w.h), dtype=torch.float32).pin_memory()
+    nbytes = sfa.decode_host_staging_bytes(w.B, w.Q, w.h, w.top_k, inp.max_blocks, w.n_splits)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    sfa.decode_host(pin(inp.q), inp.kv, pin(inp.block_table), pin(inp.seq_lens), pin(inp.topk_idx),
+                    w.scale, w.n_splits, w.Q, out_h, lse_h, staging)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())
