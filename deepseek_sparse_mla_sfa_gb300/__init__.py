@@ -24,7 +24,7 @@ MAX_HEADS = 128
 MAX_SPLITS = 64
 
 __all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
-           "workspace_bytes", "decode_launches", "last_device_status", "set_wait_limit", "SfaError", "D_QK", "D_V"]
+           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_wait_limit", "SfaError", "D_QK", "D_V"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -110,6 +110,38 @@ def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int =
     _lib.check("sfa_decode", code)
     if n_splits > 1 and not merge:
         return out_part, lse_part
+    return out, lse
+
+
+def decode_noalloc(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int = 1,
+                   Q: int = 1, out=None, lse=None, stream=None):
+    """Decode + shard merge without caller-provided scratch (C ABI ``sfa_decode_noalloc``).
+
+    For callers that cannot allocate device memory for shard partials: they live in a
+    fixed device array owned by the library (include/sfa.h, SFA_NOALLOC_SCRATCH_BYTES).
+    Pass preallocated `out` [B*Q, h, 512] and `lse` [B*Q, h] fp32 to allocate nothing here.
+    Calls that overlap on the GPU share that array and race.
+    """
+    lib = _lib.load()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _need(topk_idx, "topk_idx", torch.int32, dev, 2)
+    T, h, _ = q.shape
+    B = seq_lens.shape[0]
+    if out is None:
+        out = torch.empty((T, h, D_V), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((T, h), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, dev)
+    _need(lse, "lse", torch.float32, dev)
+    code = lib.sfa_decode_noalloc(_ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens),
+                                  _ptr(topk_idx), B, Q, h, topk_idx.shape[1], kv.shape[0],
+                                  kv.shape[1], block_table.shape[1], float(scale), n_splits,
+                                  _ptr(out), _ptr(lse), _stream_ptr(stream, dev))
+    _lib.check("sfa_decode_noalloc", code)
     return out, lse
 
 

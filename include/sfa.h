@@ -161,6 +161,35 @@ sfa_status sfa_decode_host(const void *q_host, const void *kv, const int32_t *bl
 sfa_status sfa_last_device_status(sfa_stream stream);
 
 /*
+ * sfa_decode_noalloc -- sfa_decode followed by the shard merge, for callers that
+ * cannot allocate device memory.  No passage of the source pages corresponds to
+ * it: it exists for deployments, not for the method.
+ *
+ * Some callers have no allocator: an engine that hands all free HBM to its cache
+ * pool at start-up, a plugin host that passes a library only its inputs and
+ * outputs, or a decode loop that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.  This entry point takes only the inputs and the final out/lse
+ * (layouts, alignment and argument rules as in sfa_decode; out and lse are
+ * required for every n_splits) and keeps the shard partials and any workspace in
+ * a fixed device array of SFA_NOALLOC_SCRATCH_BYTES that the library owns.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Limit: a call whose partials (n_splits > 1: n_splits*B*Q*h*513 floats, each
+ *    part rounded up to 256 bytes) plus workspace exceed SFA_NOALLOC_SCRATCH_BYTES
+ *    returns SFA_ERR_WORKSPACE and launches nothing.
+ *  - Every GPU that loads the library holds the array until the process exits.
+ *  - The first call on each device looks the array's address up (with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (other streams,
+ *    other threads) race.  Each call writes all the scratch it reads, so no
+ *    clearing between calls is needed.
+ */
+#define SFA_NOALLOC_SCRATCH_BYTES (72u << 20)
+sfa_status sfa_decode_noalloc(const void *q, const void *kv, const int32_t *block_table,
+                              const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h,
+                              int top_k, int num_blocks, int block_size, int max_blocks_per_seq,
+                              float scale, int n_splits, float *out, float *lse, sfa_stream stream);
+
+/*
  * sfa_decode_launches -- how many kernels one sfa_decode call with these
  * arguments enqueues (merge != 0: out/lse given with n_splits > 1), and through
  * *tensor_core_path whether the tcgen05 kernel serves it (1) or the CUDA-core
