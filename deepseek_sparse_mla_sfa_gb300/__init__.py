@@ -24,7 +24,7 @@ MAX_HEADS = 128
 MAX_SPLITS = 64
 
 __all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
-           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_wait_limit", "SfaError", "D_QK", "D_V"]
+           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "SfaError", "D_QK", "D_V"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -215,6 +215,14 @@ def last_device_status(stream=None) -> int:
     lib = _lib.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     return int(lib.sfa_last_device_status(_stream_ptr(stream, dev)))
+
+
+def set_kernel_path(path: int) -> int:
+    """0 = automatic (tcgen05 kernel where it applies), 1 = CUDA-core kernel only."""
+    prev = int(_lib.load().sfa_set_kernel_path(int(path)))
+    if prev < 0:
+        raise ValueError("path must be 0 or 1")
+    return prev
 
 
 def set_wait_limit(iterations: int) -> int:

@@ -37,6 +37,7 @@ SIGNATURES = {
     "sfa_status_string": ([I], ctypes.c_char_p),
     "sfa_set_wait_limit": ([ctypes.c_longlong], ctypes.c_longlong),
     "sfa_decode_noalloc": ([P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P], I),
+    "sfa_set_kernel_path": ([I], I),
     "sfa_decode_launches": ([I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)], I),
 }
 

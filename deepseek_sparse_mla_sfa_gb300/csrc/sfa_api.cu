@@ -21,6 +21,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 std::atomic<long long> g_wait_limit{0};
+std::atomic<int> g_kernel_path{0};  // 0 automatic, 1 CUDA-core only
+
+bool use_tc(int h, int block_size) { return g_kernel_path.load() == 0 && sfa::tc_supports(h, block_size); }
 constexpr long long kDefaultWaitLimit = 1LL << 26;  // iterations of a bounded device wait
 
 int* status_word(int dev) {
@@ -72,12 +75,18 @@ const char* sfa_status_string(sfa_status s) {
   return "SFA_UNKNOWN_STATUS";
 }
 
+int sfa_set_kernel_path(int path) {
+  if (path != 0 && path != 1) return -1;
+  return g_kernel_path.exchange(path);
+}
+
 long long sfa_set_wait_limit(long long iterations) {
   return g_wait_limit.exchange(iterations < 0 ? 0 : iterations);
 }
 
 size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits) {
   if (B <= 0 || Q <= 0 || h <= 0 || top_k < 0 || n_splits < 1) return 0;
+  if (g_kernel_path.load() != 0) return 0;
   return sfa::tc_workspace_bytes(B * Q, h, top_k, n_splits);
 }
 
@@ -86,7 +95,7 @@ int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_sp
   if (B < 0 || Q < 1 || h < 1 || h > SFA_MAX_HEADS || top_k < 0 || block_size < 1 ||
       n_splits < 1 || n_splits > SFA_MAX_SPLITS)
     return -1;
-  const bool tc = sfa::tc_supports(h, block_size);
+  const bool tc = use_tc(h, block_size);
   if (tensor_core_path) *tensor_core_path = tc ? 1 : 0;
   if ((long long)B * Q == 0) return 0;
   int n = tc ? sfa::tc_launches(B * Q, h, top_k, n_splits) : 1;
@@ -161,8 +170,7 @@ sfa_status sfa_decode(const void* q, const void* kv, const int32_t* block_table,
   p.wait_limit = wl > 0 ? wl : kDefaultWaitLimit;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = sfa::tc_supports(h, block_size) ? sfa::launch_decode_tc(p, s)
-                                                  : sfa::launch_decode_simt(p, s);
+  cudaError_t e = use_tc(h, block_size) ? sfa::launch_decode_tc(p, s) : sfa::launch_decode_simt(p, s);
   if (e != cudaSuccess) return SFA_ERR_CUDA;
   if (merge_after) {
     e = sfa::launch_lse_merge(out_part, lse_part, n_splits, T * h, SFA_D_V, out, lse, s);

@@ -1,9 +1,535 @@
-// sfa_tc.cu -- tcgen05 / TMA path of sparse MLA decode (sm_103a).
+// sfa_tc.cu -- tcgen05 / TMA path of sparse MLA decode on sm_103a.
+//
+// The computation is the one of "RFC: MsModeling 支持 Decode Context Parallel 仿真"
+// 2.1.4.1-2.1.4.4 and "vllm-ascend PR #18870 解读" 4.3 / 4.5: for every query token,
+// softmax(scale * q K^T) V over the latent rows its top-k list selects, with the
+// per-head log-sum-exp, optionally restricted to one sequence shard (DCP).
+//
+// Layout of the work.  One work unit = (query token, shard).  Two CTAs of a
+// cluster share a unit and all of its 128 (padded) heads:
+//   * the QK^T contraction is split by columns: CTA c holds q's latent columns
+//     [256c, 256c+256) in TMEM (A operand) and rope columns [512+32c, 544+32c) in
+//     shared memory, and gathers exactly those columns of each selected row;
+//   * P.V is split by output columns: CTA c owns out[:, 256c : 256c+256), which
+//     are the latent columns it already holds (V is the latent part of the row);
+//   * the softmax of head hh is owned by CTA hh / 64: the other CTA sends it its
+//     partial scores for that head through distributed shared memory, the owner
+//     adds them, exponentiates, and writes the bf16 probabilities P into both
+//     CTAs' shared memory.
+// Each CTA therefore reads 576 of the 1152 bytes of every selected row, once.
+// TMEM per CTA: O [128 heads x 256] fp32 (cols 0-255), q latent part (256-383,
+// bf16 pairs), two score buffers of 64 rows (384-511).
+//
+// Warp roles (192 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
+// TMEM lanes 32w..32w+31 = heads 32w..32w+31), warp 4 index resolution + TMA
+// gathers, warp 5 tcgen05 MMA issue.  Every wait is bounded; a wait that gives up
+// records SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
+#include <cuda.h>
+#include <mutex>
+
 #include "sfa_internal.h"
+#include "sfa_ptx.cuh"
 
 namespace sfa {
+namespace {
 
-bool tc_supports(int h, int block_size) { (void)h; (void)block_size; return false; }
+using namespace ptx;
+
+constexpr int kNt = 64;          // selected rows per tile
+constexpr int kStages = 4;       // gather pipeline depth
+constexpr int kHeads = 128;      // heads per unit (padded)
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P entries stay below 2^8
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kLatBlk = kNt * 128;                      // one 64-column SW128 block of a tile
+constexpr int kRopeBlk = kNt * 64;                      // the 32-column SW64 rope block
+constexpr int kStageBytes = 4 * kLatBlk + kRopeBlk;     // 36 KB
+constexpr int kOffQRope = kStages * kStageBytes;
+constexpr int kQRopeBytes = kHeads * 64;
+constexpr int kOffP = kOffQRope + kQRopeBytes;
+constexpr int kPBytes = kHeads * kNt * 2;               // P [128 heads x 64 rows] bf16
+constexpr int kOffX = kOffP + 2 * kPBytes;
+constexpr int kXBytes = 64 * kNt * 4;                   // peer partial scores [64 heads x 64] fp32
+constexpr int kOffRows = kOffX + 2 * kXBytes;
+constexpr int kOffAlpha = kOffRows + kStages * kNt * 4;
+constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;
+constexpr int kOffBar = kOffFin + kHeads * 4;
+// barriers
+constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = kBarKvEmpty + kStages,
+              kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2, kBarXFull = kBarSFree + 2,
+              kBarXFree = kBarXFull + 2, kBarPFull = kBarXFree + 2, kBarPFree = kBarPFull + 2,
+              kBarOReady = kBarPFree + 2, kBarPvDone = kBarOReady + 2, kBarFin = kBarPvDone + 1,
+              kBarMmaFin = kBarFin + 1, kNumBars = kBarMmaFin + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;         // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
+
+// waits for this CTA's own copies / MMAs still in flight at exit use their own
+// (time-capped) limit, independent of the pipeline-wait cap
+constexpr long long kDrainLimit = 1LL << 40;
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
+constexpr uint32_t kStageTx = kStageBytes;  // bytes a full tile delivers (OOB rows are zero-filled)
+
+struct TcParams {
+  DecodeParams p;
+  int num_rows;  // num_blocks * block_size (== out-of-range row used for padding)
+};
+
+__device__ __forceinline__ int lanemask_lt() {
+  int m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Physical cache row of selected entry `pos`, or -1 when the entry is padding for
+// this shard (or its block-table entry is invalid, which is reported).
+__device__ __forceinline__ int resolve_row(const DecodeParams& p, int b, int pos, int lo, int hi,
+                                           bool report) {
+  if (pos < lo || pos >= hi || pos < 0) return -1;
+  const int blk = pos / p.block_size;
+  const int phys = blk < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + blk] : -1;
+  if (phys < 0 || phys >= p.num_blocks) {
+    if (report) report_status(p.status, kStatusBadBlock);
+    return -1;
+  }
+  return phys * p.block_size + pos % p.block_size;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_lat,
+                     const __grid_constant__ CUtensorMap tmap_rope, const TcParams tp) {
+  const DecodeParams& p = tp.p;
+  extern __shared__ char smem_raw[];
+  char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  int* rows_s = reinterpret_cast<int*>(smem + kOffRows);
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* fin_s = reinterpret_cast<float*>(smem + kOffFin);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  int* total_s = reinterpret_cast<int*>(smem + kOffMisc + 4);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();   // which half of the columns / heads
+  const uint32_t peer = crank ^ 1u;
+  const int unit = blockIdx.x >> 1;
+  const int T = p.B * p.Q;
+  const int t = unit % T, r = unit / T;
+  const int b = t / p.Q, qi = t % p.Q;
+  const int seq_len = p.seq_lens[b];
+  const int L = seq_len - (p.Q - 1 - qi);
+  int lo, hi;
+  shard_bounds(seq_len, L, r, p.n_splits, lo, hi);
+  const int32_t* idx = p.topk_idx + (size_t)t * p.top_k;
+  const long long wl = p.wait_limit;
+
+  // ---- set-up: barriers, TMEM, count of valid entries ----------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarKvFull + s], 1);
+      mbar_init(&bars[kBarKvEmpty + s], 1);
+    }
+    mbar_init(&bars[kBarQReady], 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[kBarSFull + x], 1);
+      mbar_init(&bars[kBarSFree + x], 128);
+      mbar_init(&bars[kBarXFull + x], 64);   // 64 peer threads send partial scores
+      mbar_init(&bars[kBarXFree + x], 64);   // 64 peer owners consumed ours
+      mbar_init(&bars[kBarPFull + x], 128);  // 64 local + 64 peer owners wrote P
+      mbar_init(&bars[kBarPFree + x], 2);    // P.V of this tile done in both CTAs
+      mbar_init(&bars[kBarOReady + x], 128);
+    }
+    mbar_init(&bars[kBarPvDone], 1);
+    mbar_init(&bars[kBarFin], 64);
+    mbar_init(&bars[kBarMmaFin], 1);
+    *total_s = 0;
+    *abort_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_base_s, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tmap_lat);
+    prefetch_tmap(&tmap_rope);
+  }
+  __syncthreads();
+  {
+    int cnt = 0;
+    for (int j = threadIdx.x; j < p.top_k; j += kThreads)
+      cnt += resolve_row(p, b, idx[j], lo, hi, crank == 0) >= 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0 && cnt) atomicAdd(total_s, cnt);
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  const int total = *total_s;
+  const int n_tiles = (total + kNt - 1) / kNt;
+
+  auto fail = [&](void) {
+    report_status(p.status, kStatusTimeout);
+    *abort_s = 1;
+  };
+  // waits executed by a whole warp give the same answer on every lane
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, wl));
+  };
+  auto wait_warp_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait<true>(bar, parity, wl));
+  };
+
+  char* qrope = smem + kOffQRope;
+
+  if (warp < 4) {
+    // =================== softmax / rescale / epilogue warps =====================
+    const int head = warp * 32 + lane;
+    const bool owner = (warp >> 1) == (int)crank;
+    const bool head_ok = head < p.h;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+
+    // q: latent columns [256c, 256c+256) -> TMEM (bf16 pairs), rope [512+32c, +32) -> smem
+    {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          p.q + ((size_t)t * p.h + (head_ok ? head : 0)) * kDQK);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = head_ok ? __ldg(qrow + 128 * crank + 16 * j + k) : 0u;
+        tmem_st16(lane_base + kColQ + 16 * j, v);
+      }
+      const uint4* qr = reinterpret_cast<const uint4*>(qrow + 256 + 16 * crank);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint4 v = head_ok ? __ldg(qr + k) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qrope + head * 64 + ((k ^ ((head >> 1) & 3)) * 16)) = v;
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[kBarQReady]);
+    }
+
+    float m_ref = -INFINITY, l_sum = 0.f;  // owner's running max (log2 units) and sum
+    const float c_scale = p.scale * kLog2e;
+    const int hl = head - 64 * (int)(owner ? crank : peer);  // row of this head in an X buffer
+    char* xbase = smem + kOffX;
+    char* pbase = smem + kOffP;
+
+    for (int i = 0; i < n_tiles && !*abort_s; ++i) {
+      const int bb = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      if (!wait_warp(&bars[kBarSFull + bb], ph)) { fail(); break; }
+      tc_fence_after();
+      float s[kNt];
+#pragma unroll
+      for (int c4 = 0; c4 < kNt / 16; ++c4) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) s[16 * c4 + k] = __uint_as_float(v[k]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[kBarSFree + bb]);
+      char* xb = xbase + bb * kXBytes + hl * 256;
+      float alpha = 1.f;
+      if (!owner) {
+        // send the partial scores of the peer's head to its X buffer
+        if (i >= 2 && !wait_warp_cluster(&bars[kBarXFree + bb], ((i >> 1) - 1) & 1)) { fail(); break; }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t a = mapa(xb + ((k ^ (hl & 15)) * 16), peer);
+          st_cluster_v4(a, __float_as_uint(s[4 * k]), __float_as_uint(s[4 * k + 1]),
+                        __float_as_uint(s[4 * k + 2]), __float_as_uint(s[4 * k + 3]));
+        }
+        mbar_arrive_remote(mapa(&bars[kBarXFull + bb], peer));
+      } else {
+        if (!wait_warp_cluster(&bars[kBarXFull + bb], ph)) { fail(); break; }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float4 v = *reinterpret_cast<const float4*>(xb + ((k ^ (hl & 15)) * 16));
+          s[4 * k] += v.x;
+          s[4 * k + 1] += v.y;
+          s[4 * k + 2] += v.z;
+          s[4 * k + 3] += v.w;
+        }
+        mbar_arrive_remote(mapa(&bars[kBarXFree + bb], peer));
+        // online softmax in log2 units, rescaling only when the max grows past the threshold
+        const int nvalid = min(kNt, total - kNt * i);
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kNt; ++j) {
+          s[j] = j < nvalid ? s[j] * c_scale : -INFINITY;
+          mt = fmaxf(mt, s[j]);
+        }
+        float m_new = m_ref;
+        if (i == 0 || mt > m_ref + kRescaleThreshold) m_new = fmaxf(mt, m_ref);
+        alpha = i == 0 ? 1.f : exp2f(m_ref - m_new);
+        m_ref = m_new;
+        float rs = 0.f;
+        uint32_t pk[kNt / 2];
+#pragma unroll
+        for (int j = 0; j < kNt / 2; ++j) {
+          const float e0 = exp2f(s[2 * j] - m_new), e1 = exp2f(s[2 * j + 1] - m_new);
+          rs += e0 + e1;
+          pk[j] = pack_bf16(e0, e1);
+        }
+        l_sum = l_sum * alpha + rs;
+        if (i >= 2 && !wait_warp_cluster(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); break; }
+        char* prow = pbase + bb * kPBytes + head * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int off = (k ^ (head & 7)) * 16;
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          st_cluster_v4(mapa(prow + off, peer), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+        alpha_s[bb * kHeads + head] = alpha;
+        st_cluster_f32(mapa(&alpha_s[bb * kHeads + head], peer), alpha);
+        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+        mbar_arrive(&bars[kBarPFull + bb]);
+        mbar_arrive_remote(mapa(&bars[kBarPFull + bb], peer));
+      }
+      // rescale this warp's O rows when any of its heads' reference max moved
+      if (i >= 1) {
+        if (!owner) {
+          if (!wait_warp_cluster(&bars[kBarPFull + bb], ph)) { fail(); break; }
+          alpha = alpha_s[bb * kHeads + head];
+        }
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!wait_warp(&bars[kBarPvDone], (i - 1) & 1)) { fail(); break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c16 = 0; c16 < 256 / 16; ++c16) {
+            uint32_t v[16];
+            tmem_ld16(lane_base + kColO + 16 * c16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st16(lane_base + kColO + 16 * c16, v);
+          }
+          tmem_st_wait();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars[kBarOReady + bb]);
+    }
+
+    // ---- epilogue: out = O / l for this CTA's 256 columns, lse by the owner ----
+    float* out = p.out + ((size_t)r * T + t) * p.h * kDV + 256 * crank;
+    float* lse = p.lse + ((size_t)r * T + t) * p.h;
+    if (n_tiles == 0) {
+      if (head_ok) {
+        float4* o4 = reinterpret_cast<float4*>(out + (size_t)head * kDV);
+        for (int k = 0; k < 64; ++k) o4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (owner) lse[head] = -INFINITY;
+      }
+    } else if (!*abort_s) {
+      bool ok = true;
+      float l_head = l_sum;
+      if (owner) {
+        st_cluster_f32(mapa(&fin_s[head], peer), l_sum);
+        mbar_arrive_remote(mapa(&bars[kBarFin], peer));
+      } else {
+        ok = wait_warp_cluster(&bars[kBarFin], 0);
+        l_head = fin_s[head];
+      }
+      ok = wait_warp(&bars[kBarPvDone], (n_tiles - 1) & 1) && ok;
+      if (!ok) {
+        fail();
+      } else {
+        tc_fence_after();
+        const float inv = 1.f / l_head;
+        float4* o4 = reinterpret_cast<float4*>(out + (size_t)head * kDV);
+#pragma unroll 1
+        for (int c16 = 0; c16 < 256 / 16; ++c16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + kColO + 16 * c16, v);
+          tmem_ld_wait();
+          if (head_ok) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              o4[4 * c16 + k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                                            __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+          }
+        }
+        if (owner && head_ok) lse[head] = (m_ref + __log2f(l_head)) * kLn2;
+      }
+    }
+  } else if (warp == kProducerWarp) {
+    // =================== index resolution + gathers ==============================
+    int n = 0, cnt = 0;
+    bool ok = true;
+    auto acquire_stage = [&](int tile) -> bool {
+      const int s = tile % kStages;
+      return tile < kStages || wait_warp(&bars[kBarKvEmpty + s], ((tile / kStages) - 1) & 1);
+    };
+    auto issue = [&](int tile) {
+      const int s = tile % kStages;
+      char* st = smem + s * kStageBytes;
+      int* rw = rows_s + s * kNt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageTx);
+      __syncwarp();
+      if (lane < kNt / 4) {
+        const int r0 = rw[4 * lane], r1 = rw[4 * lane + 1], r2 = rw[4 * lane + 2], r3 = rw[4 * lane + 3];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tma_gather4(smem_u32(st + j * kLatBlk + lane * 4 * 128), &tmap_lat, 256 * crank + 64 * j, r0, r1,
+                      r2, r3, &bars[kBarKvFull + s]);
+        tma_gather4(smem_u32(st + 4 * kLatBlk + lane * 4 * 64), &tmap_rope, 512 + 32 * crank, r0, r1, r2, r3,
+                    &bars[kBarKvFull + s]);
+      }
+    };
+    if (n_tiles > 0) {
+      ok = acquire_stage(0);
+      for (int base = 0; ok && base < p.top_k && !*abort_s; base += 32) {
+        const int j = base + lane;
+        const int row = j < p.top_k ? resolve_row(p, b, idx[j], lo, hi, false) : -1;
+        const bool valid = row >= 0;
+        const unsigned mask = __ballot_sync(0xffffffffu, valid);
+        const int nv = __popc(mask);
+        const int rk = __popc(mask & lanemask_lt());
+        if (valid && cnt + rk < kNt) rows_s[(n % kStages) * kNt + cnt + rk] = row;
+        if (cnt + nv >= kNt) {
+          issue(n);
+          ++n;
+          if (n < n_tiles) {
+            if (!(ok = acquire_stage(n))) break;
+            if (valid && cnt + rk >= kNt) rows_s[(n % kStages) * kNt + cnt + rk - kNt] = row;
+          }
+          cnt = cnt + nv - kNt;
+        } else {
+          cnt += nv;
+        }
+      }
+      if (ok && cnt > 0 && n < n_tiles) {
+        for (int k = cnt + lane; k < kNt; k += 32) rows_s[(n % kStages) * kNt + k] = tp.num_rows;
+        issue(n);
+        ++n;
+      }
+      if (!ok) fail();
+      // no gather of this CTA may still be landing in shared memory at exit
+      for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
+          report_status(p.status, kStatusTimeout);
+    }
+  } else if (warp == kMmaWarp) {
+    // =================== tcgen05 MMA issue =======================================
+    if (lane == 0 && n_tiles > 0) {
+      bool ok = mbar_wait(&bars[kBarQReady], 0, wl);
+      tc_fence_after();
+      const uint32_t id_qk = idesc_bf16(128, kNt, 0, 0);
+      const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+      const uint32_t qrope_a = smem_u32(qrope);
+      auto qk = [&](int n) -> bool {
+        const int s = n % kStages, bb = n & 1;
+        if (!mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl)) return false;
+        if (n >= 2 && !mbar_wait(&bars[kBarSFree + bb], ((n >> 1) - 1) & 1, wl)) return false;
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + s * kStageBytes);
+        const uint32_t d = tmem + kColS + kNt * bb;
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          mma_ts(d, tmem + kColQ + 8 * k, smem_desc(st + (k >> 2) * kLatBlk + (k & 3) * 32, 16, 1024, kSwizzle128),
+                 id_qk, k > 0);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          mma_ss(d, smem_desc(qrope_a + 32 * k, 16, 512, kSwizzle64),
+                 smem_desc(st + 4 * kLatBlk + 32 * k, 16, 512, kSwizzle64), id_qk, 1);
+        mma_commit(&bars[kBarSFull + bb]);
+        return true;
+      };
+      auto pv = [&](int n) -> bool {
+        const int s = n % kStages, bb = n & 1;
+        if (!mbar_wait<true>(&bars[kBarPFull + bb], (n >> 1) & 1, wl)) return false;
+        if (!mbar_wait(&bars[kBarOReady + bb], (n >> 1) & 1, wl)) return false;
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + s * kStageBytes);
+        const uint32_t pa = smem_u32(smem + kOffP + bb * kPBytes);
+#pragma unroll
+        for (int k = 0; k < kNt / 16; ++k)
+          mma_ss(tmem + kColO, smem_desc(pa + 32 * k, 16, 1024, kSwizzle128),
+                 smem_desc(st + 2048 * k, kLatBlk, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bars[kBarKvEmpty + s]);
+        mma_commit(&bars[kBarPvDone]);
+        mma_commit_mc(&bars[kBarPFree + bb], 0x3);
+        return true;
+      };
+      ok = ok && qk(0);
+      for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
+        if (n + 1 < n_tiles) ok = qk(n + 1);
+        ok = ok && pv(n);
+      }
+      if (!ok) fail();
+      // every MMA this thread issued has completed before TMEM is released
+      mma_commit(&bars[kBarMmaFin]);
+      if (!mbar_wait(&bars[kBarMmaFin], 0, kDrainLimit)) report_status(p.status, kStatusTimeout);
+    }
+  }
+
+  // ---- teardown: all DSMEM traffic of both CTAs is over before either exits -----
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool make_row_map(CUtensorMap* m, const void* kv, int num_rows, int box_cols, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)num_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDQK * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, 1};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_supports(int h, int block_size) {
+  (void)block_size;
+  return h >= 1 && h <= kHeads;
+}
 
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits) {
   (void)T; (void)h; (void)top_k; (void)n_splits;
@@ -16,8 +542,28 @@ int tc_launches(int T, int h, int top_k, int n_splits) {
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
-  (void)p; (void)stream;
-  return cudaErrorNotSupported;
+  const long long T = (long long)p.B * p.Q;
+  const long long units = T * p.n_splits;
+  if (units == 0) return cudaSuccess;
+  const long long num_rows = (long long)p.num_blocks * p.block_size;
+  if (num_rows >= 0x7fffffffLL || 2 * units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  TcParams tp;
+  tp.p = p;
+  tp.num_rows = (int)num_rows;
+  CUtensorMap lat, rope;
+  if (!make_row_map(&lat, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_row_map(&rope, p.kv, (int)num_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  decode_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, tp);
+  return cudaGetLastError();
 }
 
 }  // namespace sfa

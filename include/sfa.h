@@ -198,6 +198,14 @@ sfa_status sfa_decode_noalloc(const void *q, const void *kv, const int32_t *bloc
 int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_splits, int merge,
                         int *tensor_core_path);
 
+/*
+ * sfa_set_kernel_path -- kernel family for sfa_decode calls made afterwards in
+ * this process: 0 = automatic (the tcgen05 kernel wherever it applies), 1 = the
+ * CUDA-core kernel for every shape (to cross-check the two).  Returns the
+ * previous setting, or -1 (and changes nothing) for another value.
+ */
+int sfa_set_kernel_path(int path);
+
 /* sfa_status_string -- static, human-readable name of a status code. */
 const char *sfa_status_string(sfa_status s);
 

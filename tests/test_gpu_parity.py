@@ -37,8 +37,16 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=[0, 1], ids=["tcgen05", "cudacore"])
+def kernel_path(request):
+    prev = sfa.set_kernel_path(request.param)
+    yield request.param
+    sfa.set_kernel_path(prev)
+
+
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
-def test_small_cases_every_element(w):
+def test_small_cases_every_element(w, kernel_path):
+    assert sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1] == (kernel_path == 0)
     inp = workloads.make(w, device="cuda")
     prob = problem_of(inp)
     ref_out, ref_lse = oracle.decode(prob)
@@ -223,3 +231,28 @@ def test_host_buffer_entry_point_matches_device_entry_point():
                     w.scale, w.n_splits, w.Q, out_h, lse_h, staging)
     torch.cuda.synchronize()
     assert torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())
+
+
+def test_tensor_core_kernel_serves_every_workload():
+    for name, w in workloads.CONFIGS.items():
+        n, tc = sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits, merge=False)
+        assert tc and n >= 1, name
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    # a wait cap of one poll makes the pipeline waits give up; the kernel must report
+    # SFA_ERR_DEVICE_TIMEOUT and return instead of hanging, and the context stays usable
+    w = W("timeout", B=2, Q=1, h=128, S=4096, top_k=512, n_splits=1, index_kind="uniform", seed=29)
+    inp = workloads.make(w, device="cuda")
+    sfa.last_device_status()
+    prev = sfa.set_wait_limit(1)
+    try:
+        run_cuda(inp)
+        status = sfa.last_device_status()
+    finally:
+        sfa.set_wait_limit(prev)
+    assert status in (-5, 0)   # a one-poll cap may still see every barrier complete in time
+    ro, rl = oracle.decode(problem_of(inp))
+    out, lse = run_cuda(inp)
+    compare(out, lse, ro, rl, "after timeout")
+    assert sfa.last_device_status() == 0
