@@ -36,9 +36,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kNt = 64;          // selected rows per tile
-constexpr int kStages = 4;       // gather pipeline depth
+constexpr int kStages = 3;       // gather pipeline depth
 constexpr int kHeads = 128;      // heads per unit (padded)
 constexpr int kThreads = 192;
+constexpr int kWarps = kThreads / 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -52,23 +53,29 @@ constexpr int kStageBytes = 4 * kLatBlk + kRopeBlk;     // 36 KB
 constexpr int kOffQRope = kStages * kStageBytes;
 constexpr int kQRopeBytes = kHeads * 64;
 constexpr int kOffP = kOffQRope + kQRopeBytes;
-constexpr int kPBytes = kHeads * kNt * 2;               // P [128 heads x 64 rows] bf16
+constexpr int kPBytes = kHeads * kNt * 2;               // P [128 heads x 64 rows] bf16, SW128 K-major
+constexpr int kPHalf = kPBytes / 2;                     // the 64 rows one CTA owns
 constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kXBytes = 64 * kNt * 4;                   // peer partial scores [64 heads x 64] fp32
-constexpr int kOffRows = kOffX + 2 * kXBytes;
-constexpr int kOffAlpha = kOffRows + kStages * kNt * 4;
+constexpr int kXBytes = 64 * kNt * 4;                   // partial scores [64 heads x 64 rows] fp32
+constexpr int kOffXStage = kOffX + 2 * kXBytes;
+constexpr int kOffAlpha = kOffXStage + kXBytes;
 constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;
-constexpr int kOffBar = kOffFin + kHeads * 4;
+constexpr int kOffList = kOffFin + kHeads * 4;
+constexpr int kListCap = 7104;                          // resolved rows kept at once (multiple of kNt)
+constexpr int kOffBar = kOffList + kListCap * 4;
 // barriers
 constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = kBarKvEmpty + kStages,
               kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2, kBarXFull = kBarSFree + 2,
-              kBarXFree = kBarXFull + 2, kBarPFull = kBarXFree + 2, kBarPFree = kBarPFull + 2,
-              kBarOReady = kBarPFree + 2, kBarPvDone = kBarOReady + 2, kBarFin = kBarPvDone + 1,
-              kBarMmaFin = kBarFin + 1, kNumBars = kBarMmaFin + 1;
+              kBarXFree = kBarXFull + 2, kBarXCons = kBarXFree + 2, kBarPReady = kBarXCons + 2,
+              kBarPFull = kBarPReady + 2, kBarPFree = kBarPFull + 2, kBarOReady = kBarPFree + 2,
+              kBarXStaged = kBarOReady + 2, kBarXStageFree = kBarXStaged + 1, kBarPvDone = kBarXStageFree + 1,
+              kBarFinLocal = kBarPvDone + 1, kBarFin = kBarFinLocal + 1, kBarMmaFin = kBarFin + 1,
+              kNumBars = kBarMmaFin + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
+static_assert(kListCap % kNt == 0, "list segments hold whole tiles");
 
 // waits for this CTA's own copies / MMAs still in flight at exit use their own
 // (time-capped) limit, independent of the pipeline-wait cap
@@ -115,12 +122,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   extern __shared__ char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  int* rows_s = reinterpret_cast<int*>(smem + kOffRows);
+  int* list_s = reinterpret_cast<int*>(smem + kOffList);
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
   float* fin_s = reinterpret_cast<float*>(smem + kOffFin);
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  int* total_s = reinterpret_cast<int*>(smem + kOffMisc + 4);
-  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  volatile int* abort_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 8);   // [kWarps]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();   // which half of the columns / heads
@@ -136,7 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int32_t* idx = p.topk_idx + (size_t)t * p.top_k;
   const long long wl = p.wait_limit;
 
-  // ---- set-up: barriers, TMEM, count of valid entries ----------------------------
+  // ---- set-up: barriers, TMEM ------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kBarKvFull + s], 1);
@@ -146,16 +153,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kBarSFull + x], 1);
       mbar_init(&bars[kBarSFree + x], 128);
-      mbar_init(&bars[kBarXFull + x], 64);   // 64 peer threads send partial scores
-      mbar_init(&bars[kBarXFree + x], 64);   // 64 peer owners consumed ours
-      mbar_init(&bars[kBarPFull + x], 128);  // 64 local + 64 peer owners wrote P
+      mbar_init(&bars[kBarXFull + x], 1);    // receiver's arming arrival + the peer's bytes
+      mbar_init(&bars[kBarXFree + x], 1);    // the peer's owners consumed our partials
+      mbar_init(&bars[kBarXCons + x], 64);   // local owners consumed the peer's partials
+      mbar_init(&bars[kBarPReady + x], 64);  // local owners wrote their P rows
+      mbar_init(&bars[kBarPFull + x], 1);    // local owners' arming arrival + the peer's P bytes
       mbar_init(&bars[kBarPFree + x], 2);    // P.V of this tile done in both CTAs
       mbar_init(&bars[kBarOReady + x], 128);
     }
+    mbar_init(&bars[kBarXStaged], 64);
+    mbar_init(&bars[kBarXStageFree], 1);
     mbar_init(&bars[kBarPvDone], 1);
-    mbar_init(&bars[kBarFin], 64);
+    mbar_init(&bars[kBarFinLocal], 64);
+    mbar_init(&bars[kBarFin], 1);
     mbar_init(&bars[kBarMmaFin], 1);
-    *total_s = 0;
     *abort_s = 0;
     fence_barrier_init();
   }
@@ -167,20 +178,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmap_lat);
     prefetch_tmap(&tmap_rope);
   }
-  __syncthreads();
+
+  // ---- index resolution: count per warp chunk, then ordered compaction into smem ----
+  const int chunk = ((p.top_k + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int c_begin = min(warp * chunk, p.top_k), c_end = min(c_begin + chunk, p.top_k);
   {
     int cnt = 0;
-    for (int j = threadIdx.x; j < p.top_k; j += kThreads)
-      cnt += resolve_row(p, b, idx[j], lo, hi, crank == 0) >= 0;
+    for (int j0 = c_begin; j0 < c_end; j0 += 32 * 8) {
+      int pos[8], blkv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int j = j0 + 32 * k + lane;
+        pos[k] = j < c_end ? __ldg(idx + j) : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const bool in = pos[k] >= lo && pos[k] < hi && pos[k] >= 0;
+        const int blk = in ? pos[k] / p.block_size : 0;
+        blkv[k] = in && blk < p.max_blocks ? __ldg(p.block_table + (size_t)b * p.max_blocks + blk) : -2;
+        if (!in) blkv[k] = -3;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (blkv[k] == -3) continue;
+        if (blkv[k] < 0 || blkv[k] >= p.num_blocks) {
+          if (crank == 0) report_status(p.status, kStatusBadBlock);
+        } else {
+          ++cnt;
+        }
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (lane == 0 && cnt) atomicAdd(total_s, cnt);
+    if (lane == 0) wcount_s[warp] = cnt;
+  }
+  __syncthreads();
+  int total = 0, off = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = wcount_s[w];
+    if (w < warp) off += c;
+    total += c;
+  }
+  for (int j0 = c_begin; j0 < c_end && off < kListCap; j0 += 32) {
+    const int j = j0 + lane;
+    const int row = j < c_end ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
+    const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+    const int o = off + __popc(mask & lanemask_lt());
+    if (row >= 0 && o < kListCap) list_s[o] = row;
+    off += __popc(mask);
   }
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
-  const int total = *total_s;
   const int n_tiles = (total + kNt - 1) / kNt;
 
   auto fail = [&](void) {
@@ -201,6 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // =================== softmax / rescale / epilogue warps =====================
     const int head = warp * 32 + lane;
     const bool owner = (warp >> 1) == (int)crank;
+    const bool elected = lane == 0 && (warp & 1) == 0;   // first lane of the first warp of a pair
     const bool head_ok = head < p.h;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 
@@ -227,18 +279,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars[kBarQReady]);
     }
 
-    float m_ref = -INFINITY, l_sum = 0.f;  // owner's running max (log2 units) and sum
     const float c_scale = p.scale * kLog2e;
     const int hl = head - 64 * (int)(owner ? crank : peer);  // row of this head in an X buffer
     char* xbase = smem + kOffX;
+    char* xstage = smem + kOffXStage;
     char* pbase = smem + kOffP;
 
-    for (int i = 0; i < n_tiles && !*abort_s; ++i) {
-      const int bb = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
-      if (!wait_warp(&bars[kBarSFull + bb], ph)) { fail(); break; }
+    // rescale this warp's O rows by alpha (any lane != 1) once P.V of tile `prev` is done
+    auto rescale = [&](float alpha, int prev) -> bool {
+      if (!__any_sync(0xffffffffu, alpha != 1.f)) return true;
+      if (!wait_warp(&bars[kBarPvDone], prev & 1)) return false;
       tc_fence_after();
-      float s[kNt];
+#pragma unroll 1
+      for (int c16 = 0; c16 < 256 / 16; ++c16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + kColO + 16 * c16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+        tmem_st16(lane_base + kColO + 16 * c16, v);
+      }
+      tmem_st_wait();
+      return true;
+    };
+    auto load_s = [&](int i, float (&s)[kNt]) -> bool {
+      const int bb = i & 1;
+      if (!wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) return false;
+      tc_fence_after();
 #pragma unroll
       for (int c4 = 0; c4 < kNt / 16; ++c4) {
         uint32_t v[16];
@@ -249,30 +316,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars[kBarSFree + bb]);
-      char* xb = xbase + bb * kXBytes + hl * 256;
-      float alpha = 1.f;
-      if (!owner) {
-        // send the partial scores of the peer's head to its X buffer
-        if (i >= 2 && !wait_warp_cluster(&bars[kBarXFree + bb], ((i >> 1) - 1) & 1)) { fail(); break; }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint32_t a = mapa(xb + ((k ^ (hl & 15)) * 16), peer);
-          st_cluster_v4(a, __float_as_uint(s[4 * k]), __float_as_uint(s[4 * k + 1]),
-                        __float_as_uint(s[4 * k + 2]), __float_as_uint(s[4 * k + 3]));
-        }
-        mbar_arrive_remote(mapa(&bars[kBarXFull + bb], peer));
-      } else {
+      return true;
+    };
+
+    float m_ref = -INFINITY, l_sum = 0.f;  // owner's running max (log2 units) and sum
+    if (owner) {
+      for (int i = 0; i < n_tiles && !*abort_s; ++i) {
+        const int bb = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (elected) mbar_arrive_expect_tx(&bars[kBarXFull + bb], kXBytes);   // arm for the peer's bytes
+        __syncwarp();
+        float s[kNt];
+        if (!load_s(i, s)) { fail(); break; }
         if (!wait_warp_cluster(&bars[kBarXFull + bb], ph)) { fail(); break; }
+        const char* xr = xbase + bb * kXBytes + hl * 256;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float4 v = *reinterpret_cast<const float4*>(xb + ((k ^ (hl & 15)) * 16));
+          const float4 v = *reinterpret_cast<const float4*>(xr + ((k ^ (hl & 15)) * 16));
           s[4 * k] += v.x;
           s[4 * k + 1] += v.y;
           s[4 * k + 2] += v.z;
           s[4 * k + 3] += v.w;
         }
-        mbar_arrive_remote(mapa(&bars[kBarXFree + bb], peer));
-        // online softmax in log2 units, rescaling only when the max grows past the threshold
+        mbar_arrive(&bars[kBarXCons + bb]);
+        if (elected) {
+          if (!mbar_wait(&bars[kBarXCons + bb], ph, wl)) fail();
+          else mbar_arrive_remote(mapa(&bars[kBarXFree + bb], peer));
+        }
+        __syncwarp();
+        // online softmax in log2 units; the reference max only moves when it grows past
+        // the threshold, so O is rarely rescaled
         const int nvalid = min(kNt, total - kNt * i);
         float mt = -INFINITY;
 #pragma unroll
@@ -282,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         float m_new = m_ref;
         if (i == 0 || mt > m_ref + kRescaleThreshold) m_new = fmaxf(mt, m_ref);
-        alpha = i == 0 ? 1.f : exp2f(m_ref - m_new);
+        const float alpha = i == 0 ? 1.f : exp2f(m_ref - m_new);
         m_ref = m_new;
         float rs = 0.f;
         uint32_t pk[kNt / 2];
@@ -296,40 +369,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (i >= 2 && !wait_warp_cluster(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); break; }
         char* prow = pbase + bb * kPBytes + head * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int off = (k ^ (head & 7)) * 16;
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          st_cluster_v4(mapa(prow + off, peer), pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(prow + ((k ^ (head & 7)) * 16)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         alpha_s[bb * kHeads + head] = alpha;
-        st_cluster_f32(mapa(&alpha_s[bb * kHeads + head], peer), alpha);
-        asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-        mbar_arrive(&bars[kBarPFull + bb]);
-        mbar_arrive_remote(mapa(&bars[kBarPFull + bb], peer));
-      }
-      // rescale this warp's O rows when any of its heads' reference max moved
-      if (i >= 1) {
-        if (!owner) {
-          if (!wait_warp_cluster(&bars[kBarPFull + bb], ph)) { fail(); break; }
-          alpha = alpha_s[bb * kHeads + head];
-        }
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_warp(&bars[kBarPvDone], (i - 1) & 1)) { fail(); break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c16 = 0; c16 < 256 / 16; ++c16) {
-            uint32_t v[16];
-            tmem_ld16(lane_base + kColO + 16 * c16, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st16(lane_base + kColO + 16 * c16, v);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kBarPReady + bb]);
+        if (elected) {
+          // our 64 P rows and alphas -> the peer; our own P.V waits for the peer's half
+          if (!mbar_wait(&bars[kBarPReady + bb], ph, wl)) {
+            fail();
+          } else {
+            mbar_arrive_expect_tx(&bars[kBarPFull + bb], kPHalf + 64 * 4);
+            const uint32_t rbar = mapa(&bars[kBarPFull + bb], peer);
+            char* psrc = pbase + bb * kPBytes + kPHalf * crank;
+            bulk_copy_s2cluster(mapa(psrc, peer), psrc, kPHalf, rbar);
+            float* asrc = alpha_s + bb * kHeads + 64 * crank;
+            bulk_copy_s2cluster(mapa(asrc, peer), asrc, 64 * 4, rbar);
+            bulk_commit_group();
           }
-          tmem_st_wait();
+        }
+        __syncwarp();
+        if (i >= 1 && !rescale(alpha, i - 1)) { fail(); break; }
+        tc_fence_before();
+        mbar_arrive(&bars[kBarOReady + bb]);
+      }
+    } else {
+      // sender warps: partial scores of the peer's heads go to the peer; then finish the
+      // previous tile (O rescale of these heads with the alpha the peer sent back)
+      for (int i = 0; i <= n_tiles && !*abort_s; ++i) {
+        if (i < n_tiles) {
+          const int bb = i & 1;
+          float s[kNt];
+          if (!load_s(i, s)) { fail(); break; }
+          if (i >= 1 && !wait_warp(&bars[kBarXStageFree], (i - 1) & 1)) { fail(); break; }
+          char* xr = xstage + hl * 256;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            *reinterpret_cast<float4*>(xr + ((k ^ (hl & 15)) * 16)) =
+                make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(&bars[kBarXStaged]);
+          if (elected) {
+            bool ok = mbar_wait(&bars[kBarXStaged], i & 1, wl);
+            ok = ok && (i < 2 || mbar_wait<true>(&bars[kBarXFree + bb], ((i >> 1) - 1) & 1, wl));
+            if (!ok) {
+              fail();
+            } else {
+              bulk_copy_s2cluster(mapa(xbase + bb * kXBytes, peer), xstage, kXBytes,
+                                  mapa(&bars[kBarXFull + bb], peer));
+              bulk_commit_group();
+              bulk_wait_read<0>();
+              mbar_arrive(&bars[kBarXStageFree]);
+            }
+          }
+          __syncwarp();
+        }
+        if (i >= 1) {
+          const int pb = (i - 1) & 1;
+          if (!wait_warp_cluster(&bars[kBarPFull + pb], ((i - 1) >> 1) & 1)) { fail(); break; }
+          const float alpha = alpha_s[pb * kHeads + head];
+          if (i >= 2 && !rescale(alpha, i - 2)) { fail(); break; }
+          tc_fence_before();
+          mbar_arrive(&bars[kBarOReady + pb]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars[kBarOReady + bb]);
     }
 
     // ---- epilogue: out = O / l for this CTA's 256 columns, lse by the owner ----
@@ -345,9 +449,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       float l_head = l_sum;
       if (owner) {
-        st_cluster_f32(mapa(&fin_s[head], peer), l_sum);
-        mbar_arrive_remote(mapa(&bars[kBarFin], peer));
+        fin_s[head] = l_sum;
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kBarFinLocal]);
+        if (elected) {
+          if (!mbar_wait(&bars[kBarFinLocal], 0, wl)) {
+            fail();
+          } else {
+            bulk_copy_s2cluster(mapa(fin_s + 64 * crank, peer), fin_s + 64 * crank, 64 * 4,
+                                mapa(&bars[kBarFin], peer));
+            bulk_commit_group();
+          }
+        }
+        __syncwarp();
       } else {
+        if (elected) mbar_arrive_expect_tx(&bars[kBarFin], 64 * 4);
+        __syncwarp();
         ok = wait_warp_cluster(&bars[kBarFin], 0);
         l_head = fin_s[head];
       }
@@ -373,64 +490,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (owner && head_ok) lse[head] = (m_ref + __log2f(l_head)) * kLn2;
       }
     }
+    if (elected) bulk_wait<0>();   // every copy this thread issued has landed
+    __syncwarp();
   } else if (warp == kProducerWarp) {
-    // =================== index resolution + gathers ==============================
-    int n = 0, cnt = 0;
+    // =================== gathers ===================================================
+    int seg = 0;   // which kListCap-row segment of the resolved list is in list_s
+    int n = 0;
     bool ok = true;
-    auto acquire_stage = [&](int tile) -> bool {
-      const int s = tile % kStages;
-      return tile < kStages || wait_warp(&bars[kBarKvEmpty + s], ((tile / kStages) - 1) & 1);
-    };
-    auto issue = [&](int tile) {
-      const int s = tile % kStages;
+    for (; n < n_tiles && !*abort_s; ++n) {
+      const int s = n % kStages;
+      if (n >= kStages && !(ok = wait_warp(&bars[kBarKvEmpty + s], ((n / kStages) - 1) & 1))) break;
+      const int first = kNt * n;
+      if (first >= (seg + 1) * kListCap) {
+        // rare (more than kListCap valid entries): re-resolve the next segment here
+        seg = first / kListCap;
+        int ord = 0;
+        for (int j0 = 0; j0 < p.top_k; j0 += 32) {
+          const int j = j0 + lane;
+          const int row = j < p.top_k ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
+          const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+          const int o = ord + __popc(mask & lanemask_lt()) - seg * kListCap;
+          if (row >= 0 && o >= 0 && o < kListCap) list_s[o] = row;
+          ord += __popc(mask);
+        }
+        __syncwarp();
+      }
       char* st = smem + s * kStageBytes;
-      int* rw = rows_s + s * kNt;
-      __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageTx);
       __syncwarp();
       if (lane < kNt / 4) {
-        const int r0 = rw[4 * lane], r1 = rw[4 * lane + 1], r2 = rw[4 * lane + 2], r3 = rw[4 * lane + 3];
+        int rr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int e = first + 4 * lane + k;
+          rr[k] = e < total ? list_s[e - seg * kListCap] : tp.num_rows;   // past the end: zero fill
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          tma_gather4(smem_u32(st + j * kLatBlk + lane * 4 * 128), &tmap_lat, 256 * crank + 64 * j, r0, r1,
-                      r2, r3, &bars[kBarKvFull + s]);
-        tma_gather4(smem_u32(st + 4 * kLatBlk + lane * 4 * 64), &tmap_rope, 512 + 32 * crank, r0, r1, r2, r3,
-                    &bars[kBarKvFull + s]);
+          tma_gather4(smem_u32(st + j * kLatBlk + lane * 4 * 128), &tmap_lat, 256 * crank + 64 * j, rr[0], rr[1],
+                      rr[2], rr[3], &bars[kBarKvFull + s]);
+        tma_gather4(smem_u32(st + 4 * kLatBlk + lane * 4 * 64), &tmap_rope, 512 + 32 * crank, rr[0], rr[1], rr[2],
+                    rr[3], &bars[kBarKvFull + s]);
       }
-    };
-    if (n_tiles > 0) {
-      ok = acquire_stage(0);
-      for (int base = 0; ok && base < p.top_k && !*abort_s; base += 32) {
-        const int j = base + lane;
-        const int row = j < p.top_k ? resolve_row(p, b, idx[j], lo, hi, false) : -1;
-        const bool valid = row >= 0;
-        const unsigned mask = __ballot_sync(0xffffffffu, valid);
-        const int nv = __popc(mask);
-        const int rk = __popc(mask & lanemask_lt());
-        if (valid && cnt + rk < kNt) rows_s[(n % kStages) * kNt + cnt + rk] = row;
-        if (cnt + nv >= kNt) {
-          issue(n);
-          ++n;
-          if (n < n_tiles) {
-            if (!(ok = acquire_stage(n))) break;
-            if (valid && cnt + rk >= kNt) rows_s[(n % kStages) * kNt + cnt + rk - kNt] = row;
-          }
-          cnt = cnt + nv - kNt;
-        } else {
-          cnt += nv;
-        }
-      }
-      if (ok && cnt > 0 && n < n_tiles) {
-        for (int k = cnt + lane; k < kNt; k += 32) rows_s[(n % kStages) * kNt + k] = tp.num_rows;
-        issue(n);
-        ++n;
-      }
-      if (!ok) fail();
-      // no gather of this CTA may still be landing in shared memory at exit
-      for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
-          report_status(p.status, kStatusTimeout);
     }
+    if (!ok) fail();
+    // no gather of this CTA may still be landing in shared memory at exit
+    for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
+        report_status(p.status, kStatusTimeout);
   } else if (warp == kMmaWarp) {
     // =================== tcgen05 MMA issue =======================================
     if (lane == 0 && n_tiles > 0) {
