@@ -38,10 +38,12 @@ using namespace ptx;
 constexpr int kNt = 64;          // selected rows per tile
 constexpr int kStages = 3;       // gather pipeline depth
 constexpr int kHeads = 128;      // heads per unit (padded)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kWarps = kThreads / 32;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kProducerWarp = 4;  // warps 4..7 issue the gathers (one lane each)
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 8;        // issues QK^T
+constexpr int kPvWarp = 9;         // issues P.V
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P entries stay below 2^8
@@ -66,11 +68,12 @@ constexpr int kOffBar = kOffList + kListCap * 4;
 // barriers
 constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = kBarKvEmpty + kStages,
               kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2, kBarXFull = kBarSFree + 2,
-              kBarXFree = kBarXFull + 2, kBarXCons = kBarXFree + 2, kBarPReady = kBarXCons + 2,
+              kBarPReady = kBarXFull + 2,
               kBarPFull = kBarPReady + 2, kBarPFree = kBarPFull + 2, kBarOReady = kBarPFree + 2,
               kBarXStaged = kBarOReady + 2, kBarXStageFree = kBarXStaged + 1, kBarPvDone = kBarXStageFree + 1,
               kBarFinLocal = kBarPvDone + 1, kBarFin = kBarFinLocal + 1, kBarMmaFin = kBarFin + 1,
-              kNumBars = kBarMmaFin + 1;
+              kBarMmaFin2 = kBarMmaFin + 1, kBarPvFinal = kBarMmaFin2 + 1,
+              kNumBars = kBarPvFinal + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -94,6 +97,13 @@ __device__ __forceinline__ int lanemask_lt() {
   int m;
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
+}
+
+// 2^x on the special-function unit (inputs <= 8 here; -inf gives 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -146,7 +156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, TMEM ------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[kBarKvFull + s], 1);
+      mbar_init(&bars[kBarKvFull + s], kProducerWarps);
       mbar_init(&bars[kBarKvEmpty + s], 1);
     }
     mbar_init(&bars[kBarQReady], 128);
@@ -154,8 +164,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarSFull + x], 1);
       mbar_init(&bars[kBarSFree + x], 128);
       mbar_init(&bars[kBarXFull + x], 1);    // receiver's arming arrival + the peer's bytes
-      mbar_init(&bars[kBarXFree + x], 1);    // the peer's owners consumed our partials
-      mbar_init(&bars[kBarXCons + x], 64);   // local owners consumed the peer's partials
       mbar_init(&bars[kBarPReady + x], 64);  // local owners wrote their P rows
       mbar_init(&bars[kBarPFull + x], 1);    // local owners' arming arrival + the peer's P bytes
       mbar_init(&bars[kBarPFree + x], 2);    // P.V of this tile done in both CTAs
@@ -167,6 +175,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarFinLocal], 64);
     mbar_init(&bars[kBarFin], 1);
     mbar_init(&bars[kBarMmaFin], 1);
+    mbar_init(&bars[kBarMmaFin2], 1);
+    mbar_init(&bars[kBarPvFinal], 1);   // the last P.V of the unit has completed
     *abort_s = 0;
     fence_barrier_init();
   }
@@ -174,7 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_base_s, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
+  if (warp >= kProducerWarp && warp < kProducerWarp + kProducerWarps && lane == 0) {
     prefetch_tmap(&tmap_lat);
     prefetch_tmap(&tmap_rope);
   }
@@ -280,6 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c_scale = p.scale * kLog2e;
+    const float c_abs = fabsf(c_scale);
     const int hl = head - 64 * (int)(owner ? crank : peer);  // row of this head in an X buffer
     char* xbase = smem + kOffX;
     char* xstage = smem + kOffXStage;
@@ -338,33 +349,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[4 * k + 2] += v.z;
           s[4 * k + 3] += v.w;
         }
-        mbar_arrive(&bars[kBarXCons + bb]);
-        if (elected) {
-          if (!mbar_wait(&bars[kBarXCons + bb], ph, wl)) fail();
-          else mbar_arrive_remote(mapa(&bars[kBarXFree + bb], peer));
-        }
-        __syncwarp();
         // online softmax in log2 units; the reference max only moves when it grows past
         // the threshold, so O is rarely rescaled
         const int nvalid = min(kNt, total - kNt * i);
-        float mt = -INFINITY;
+        if (c_scale < 0.f) {   // keep max(s) * |c| == max(s * c) for a negative scale
 #pragma unroll
-        for (int j = 0; j < kNt; ++j) {
-          s[j] = j < nvalid ? s[j] * c_scale : -INFINITY;
-          mt = fmaxf(mt, s[j]);
+          for (int j = 0; j < kNt; ++j) s[j] = -s[j];
         }
+        if (nvalid < kNt) {
+#pragma unroll
+          for (int j = 0; j < kNt; ++j)
+            if (j >= nvalid) s[j] = -INFINITY;
+        }
+        float mx[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(s[4 * j], s[4 * j + 1]), fmaxf(s[4 * j + 2], s[4 * j + 3]));
+#pragma unroll
+        for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+          for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
+        const float mt = mx[0] * c_abs;
         float m_new = m_ref;
         if (i == 0 || mt > m_ref + kRescaleThreshold) m_new = fmaxf(mt, m_ref);
-        const float alpha = i == 0 ? 1.f : exp2f(m_ref - m_new);
+        const float alpha = i == 0 ? 1.f : ex2(m_ref - m_new);
         m_ref = m_new;
-        float rs = 0.f;
         uint32_t pk[kNt / 2];
+        float sm[16];
 #pragma unroll
         for (int j = 0; j < kNt / 2; ++j) {
-          const float e0 = exp2f(s[2 * j] - m_new), e1 = exp2f(s[2 * j + 1] - m_new);
-          rs += e0 + e1;
+          const float e0 = ex2(fmaf(s[2 * j], c_abs, -m_new));
+          const float e1 = ex2(fmaf(s[2 * j + 1], c_abs, -m_new));
+          if (j < 16) sm[j] = e0 + e1; else sm[j - 16] += e0 + e1;
           pk[j] = pack_bf16(e0, e1);
         }
+#pragma unroll
+        for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+          for (int j = 0; j < w2; ++j) sm[j] += sm[j + w2];
+        const float rs = sm[0];
         l_sum = l_sum * alpha + rs;
         if (i >= 2 && !wait_warp_cluster(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); break; }
         char* prow = pbase + bb * kPBytes + head * 128;
@@ -395,11 +417,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[kBarOReady + bb]);
       }
     } else {
-      // sender warps: partial scores of the peer's heads go to the peer; then finish the
-      // previous tile (O rescale of these heads with the alpha the peer sent back)
-      for (int i = 0; i <= n_tiles && !*abort_s; ++i) {
-        if (i < n_tiles) {
-          const int bb = i & 1;
+      // sender warps: two streams of work, handled in whichever order they become ready:
+      //   send(ns):   partial scores of the peer's heads for tile ns -> the peer's X buffer
+      //   finish(nf): once the peer's P / alpha of tile nf landed, rescale these heads' O
+      //               rows if their reference max moved, and release P.V of tile nf
+      // (finishing never waits behind a late gather of a later tile)
+      int ns = 0, nf = 0;
+      long long idle = 0;
+      const uint64_t t_start = globaltimer_ns();
+      while (nf < n_tiles && !*abort_s) {
+        bool progressed = false;
+        if (ns < n_tiles && ns <= nf + 1 &&
+            __all_sync(0xffffffffu, mbar_test(&bars[kBarSFull + (ns & 1)], (ns >> 1) & 1))) {
+          const int i = ns, bb = i & 1;
           float s[kNt];
           if (!load_s(i, s)) { fail(); break; }
           if (i >= 1 && !wait_warp(&bars[kBarXStageFree], (i - 1) & 1)) { fail(); break; }
@@ -412,7 +442,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars[kBarXStaged]);
           if (elected) {
             bool ok = mbar_wait(&bars[kBarXStaged], i & 1, wl);
-            ok = ok && (i < 2 || mbar_wait<true>(&bars[kBarXFree + bb], ((i >> 1) - 1) & 1, wl));
+            // the peer's X buffer bb was read by the peer's owners for tile i-2 before
+            // they sent us their P of that tile: P(i-2) landing here frees the buffer
+            ok = ok && (i < 2 || mbar_wait<true>(&bars[kBarPFull + bb], ((i >> 1) - 1) & 1, wl));
             if (!ok) {
               fail();
             } else {
@@ -424,14 +456,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           __syncwarp();
+          ++ns;
+          progressed = true;
         }
-        if (i >= 1) {
-          const int pb = (i - 1) & 1;
-          if (!wait_warp_cluster(&bars[kBarPFull + pb], ((i - 1) >> 1) & 1)) { fail(); break; }
+        if (nf < ns && __all_sync(0xffffffffu, mbar_test_cluster(&bars[kBarPFull + (nf & 1)], (nf >> 1) & 1))) {
+          const int pb = nf & 1;
           const float alpha = alpha_s[pb * kHeads + head];
-          if (i >= 2 && !rescale(alpha, i - 2)) { fail(); break; }
+          if (nf >= 1 && !rescale(alpha, nf - 1)) { fail(); break; }
           tc_fence_before();
           mbar_arrive(&bars[kBarOReady + pb]);
+          ++nf;
+          progressed = true;
+        }
+        if (!progressed) {
+          if (++idle >= wl || ((idle & 1023) == 0 && globaltimer_ns() - t_start > 4000000000ull)) { fail(); break; }
+          __nanosleep(20);
         }
       }
     }
@@ -468,7 +507,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = wait_warp_cluster(&bars[kBarFin], 0);
         l_head = fin_s[head];
       }
-      ok = wait_warp(&bars[kBarPvDone], (n_tiles - 1) & 1) && ok;
+      // a dedicated one-phase barrier: pv_done may still be two phases behind here
+      ok = wait_warp(&bars[kBarPvFinal], 0) && ok;
       if (!ok) {
         fail();
       } else {
@@ -492,8 +532,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (elected) bulk_wait<0>();   // every copy this thread issued has landed
     __syncwarp();
-  } else if (warp == kProducerWarp) {
+  } else if (warp < kProducerWarp + kProducerWarps) {
     // =================== gathers ===================================================
+    // Producer warp pw issues, from one lane, the gathers of row groups g = pw, pw+4,
+    // .. (4 rows each) of every tile: a single TMA-issuing lane per warp and several
+    // warps in parallel keep the gather engine busiest.
+    const int pw = warp - kProducerWarp;
     int seg = 0;   // which kListCap-row segment of the resolved list is in list_s
     int n = 0;
     bool ok = true;
@@ -502,7 +546,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (n >= kStages && !(ok = wait_warp(&bars[kBarKvEmpty + s], ((n / kStages) - 1) & 1))) break;
       const int first = kNt * n;
       if (first >= (seg + 1) * kListCap) {
-        // rare (more than kListCap valid entries): re-resolve the next segment here
+        // rare (more than kListCap valid entries): this warp re-resolves the entries of
+        // its own row groups for the next segment (disjoint writes, no cross-warp sync)
         seg = first / kListCap;
         int ord = 0;
         for (int j0 = 0; j0 < p.top_k; j0 += 32) {
@@ -510,85 +555,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int row = j < p.top_k ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
           const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
           const int o = ord + __popc(mask & lanemask_lt()) - seg * kListCap;
-          if (row >= 0 && o >= 0 && o < kListCap) list_s[o] = row;
+          if (row >= 0 && o >= 0 && o < kListCap && ((o % kNt) / 4) % kProducerWarps == pw) list_s[o] = row;
           ord += __popc(mask);
         }
         __syncwarp();
       }
-      char* st = smem + s * kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageTx);
-      __syncwarp();
-      if (lane < kNt / 4) {
-        int rr[4];
+      if (lane == 0) {
+        char* st = smem + s * kStageBytes;
+        mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageTx / kProducerWarps);
+#pragma unroll 1
+        for (int g = pw; g < kNt / 4; g += kProducerWarps) {
+          int rr[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int e = first + 4 * lane + k;
-          rr[k] = e < total ? list_s[e - seg * kListCap] : tp.num_rows;   // past the end: zero fill
+          for (int k = 0; k < 4; ++k) {
+            const int e = first + 4 * g + k;
+            rr[k] = e < total ? list_s[e - seg * kListCap] : tp.num_rows;   // past the end: zero fill
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_gather4(smem_u32(st + j * kLatBlk + g * 4 * 128), &tmap_lat, 256 * crank + 64 * j, rr[0], rr[1], rr[2],
+                        rr[3], &bars[kBarKvFull + s]);
+          tma_gather4(smem_u32(st + 4 * kLatBlk + g * 4 * 64), &tmap_rope, 512 + 32 * crank, rr[0], rr[1], rr[2], rr[3],
+                      &bars[kBarKvFull + s]);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tma_gather4(smem_u32(st + j * kLatBlk + lane * 4 * 128), &tmap_lat, 256 * crank + 64 * j, rr[0], rr[1],
-                      rr[2], rr[3], &bars[kBarKvFull + s]);
-        tma_gather4(smem_u32(st + 4 * kLatBlk + lane * 4 * 64), &tmap_rope, 512 + 32 * crank, rr[0], rr[1], rr[2],
-                    rr[3], &bars[kBarKvFull + s]);
       }
+      __syncwarp();
     }
     if (!ok) fail();
     // no gather of this CTA may still be landing in shared memory at exit
     for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
         report_status(p.status, kStatusTimeout);
-  } else if (warp == kMmaWarp) {
-    // =================== tcgen05 MMA issue =======================================
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // =================== tcgen05 MMA issue: QK^T (warp 5) and P.V (warp 6) ========
+    // Two issuing threads, so that QK^T of later tiles never waits behind a P.V that
+    // is still waiting for its probabilities.
     if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(&bars[kBarQReady], 0, wl);
-      tc_fence_after();
-      const uint32_t id_qk = idesc_bf16(128, kNt, 0, 0);
-      const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
-      const uint32_t qrope_a = smem_u32(qrope);
-      auto qk = [&](int n) -> bool {
-        const int s = n % kStages, bb = n & 1;
-        if (!mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl)) return false;
-        if (n >= 2 && !mbar_wait(&bars[kBarSFree + bb], ((n >> 1) - 1) & 1, wl)) return false;
+      bool ok = true;
+      if (warp == kMmaWarp) {
+        ok = mbar_wait(&bars[kBarQReady], 0, wl);
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + s * kStageBytes);
-        const uint32_t d = tmem + kColS + kNt * bb;
+        const uint32_t id_qk = idesc_bf16(128, kNt, 0, 0);
+        const uint32_t qrope_a = smem_u32(qrope);
+        for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
+          const int s = n % kStages, bb = n & 1;
+          if (!(ok = mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl))) break;
+          if (n >= 2 && !(ok = mbar_wait(&bars[kBarSFree + bb], ((n >> 1) - 1) & 1, wl))) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * kStageBytes);
+          const uint32_t d = tmem + kColS + kNt * bb;
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          mma_ts(d, tmem + kColQ + 8 * k, smem_desc(st + (k >> 2) * kLatBlk + (k & 3) * 32, 16, 1024, kSwizzle128),
-                 id_qk, k > 0);
+          for (int k = 0; k < 16; ++k)
+            mma_ts(d, tmem + kColQ + 8 * k,
+                   smem_desc(st + (k >> 2) * kLatBlk + (k & 3) * 32, 16, 1024, kSwizzle128), id_qk, k > 0);
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-          mma_ss(d, smem_desc(qrope_a + 32 * k, 16, 512, kSwizzle64),
-                 smem_desc(st + 4 * kLatBlk + 32 * k, 16, 512, kSwizzle64), id_qk, 1);
-        mma_commit(&bars[kBarSFull + bb]);
-        return true;
-      };
-      auto pv = [&](int n) -> bool {
-        const int s = n % kStages, bb = n & 1;
-        if (!mbar_wait<true>(&bars[kBarPFull + bb], (n >> 1) & 1, wl)) return false;
-        if (!mbar_wait(&bars[kBarOReady + bb], (n >> 1) & 1, wl)) return false;
-        tc_fence_after();
-        const uint32_t st = smem_u32(smem + s * kStageBytes);
-        const uint32_t pa = smem_u32(smem + kOffP + bb * kPBytes);
+          for (int k = 0; k < 2; ++k)
+            mma_ss(d, smem_desc(qrope_a + 32 * k, 16, 512, kSwizzle64),
+                   smem_desc(st + 4 * kLatBlk + 32 * k, 16, 512, kSwizzle64), id_qk, 1);
+          mma_commit(&bars[kBarSFull + bb]);
+        }
+      } else {
+        const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+        for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
+          const int s = n % kStages, bb = n & 1;
+          if (!(ok = mbar_wait<true>(&bars[kBarPFull + bb], (n >> 1) & 1, wl))) break;
+          if (!(ok = mbar_wait(&bars[kBarOReady + bb], (n >> 1) & 1, wl))) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * kStageBytes);
+          const uint32_t pa = smem_u32(smem + kOffP + bb * kPBytes);
 #pragma unroll
-        for (int k = 0; k < kNt / 16; ++k)
-          mma_ss(tmem + kColO, smem_desc(pa + 32 * k, 16, 1024, kSwizzle128),
-                 smem_desc(st + 2048 * k, kLatBlk, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bars[kBarKvEmpty + s]);
-        mma_commit(&bars[kBarPvDone]);
-        mma_commit_mc(&bars[kBarPFree + bb], 0x3);
-        return true;
-      };
-      ok = ok && qk(0);
-      for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
-        if (n + 1 < n_tiles) ok = qk(n + 1);
-        ok = ok && pv(n);
+          for (int k = 0; k < kNt / 16; ++k)
+            mma_ss(tmem + kColO, smem_desc(pa + 32 * k, 16, 1024, kSwizzle128),
+                   smem_desc(st + 2048 * k, kLatBlk, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars[kBarKvEmpty + s]);
+          mma_commit(&bars[kBarPvDone]);
+          mma_commit_mc(&bars[kBarPFree + bb], 0x3);
+          if (n == n_tiles - 1) mma_commit(&bars[kBarPvFinal]);
+        }
       }
       if (!ok) fail();
       // every MMA this thread issued has completed before TMEM is released
-      mma_commit(&bars[kBarMmaFin]);
-      if (!mbar_wait(&bars[kBarMmaFin], 0, kDrainLimit)) report_status(p.status, kStatusTimeout);
+      uint64_t* fin_bar = &bars[warp == kMmaWarp ? kBarMmaFin : kBarMmaFin2];
+      mma_commit(fin_bar);
+      if (!mbar_wait(fin_bar, 0, kDrainLimit)) report_status(p.status, kStatusTimeout);
     }
   }
 
