@@ -387,9 +387,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's B (smaller cases for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.batch:
+        import dataclasses
+        w = dataclasses.replace(workloads.CONFIGS[args.config], B=args.batch,
+                                name=f"{args.config}_b{args.batch}")
+        workloads.CONFIGS[w.name] = w
+        args.config = w.name
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":
