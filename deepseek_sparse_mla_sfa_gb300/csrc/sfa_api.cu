@@ -8,7 +8,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/sfa.h"
+#include "sfa.h"
 #include "sfa_internal.h"
 
 namespace {

@@ -17,7 +17,7 @@
 // two threads) share the one array and race.
 #include <mutex>
 
-#include "../../include/sfa.h"
+#include "sfa.h"
 #include "sfa_internal.h"
 
 namespace {

@@ -10,20 +10,21 @@
 //   * the QK^T contraction is split by columns: CTA c holds q's latent columns
 //     [256c, 256c+256) in TMEM (A operand) and rope columns [512+32c, 544+32c) in
 //     shared memory, and gathers exactly those columns of each selected row;
+//   * each CTA sends the other its partial scores for all heads through
+//     distributed shared memory; both then hold the full scores S = S_0 + S_1
+//     (the same fp32 sums in both CTAs) and run the same online softmax, so their
+//     probabilities, running max and sum agree bit for bit without exchanging them;
 //   * P.V is split by output columns: CTA c owns out[:, 256c : 256c+256), which
-//     are the latent columns it already holds (V is the latent part of the row);
-//   * the softmax of head hh is owned by CTA hh / 64: the other CTA sends it its
-//     partial scores for that head through distributed shared memory, the owner
-//     adds them, exponentiates, and writes the bf16 probabilities P into both
-//     CTAs' shared memory.
+//     are the latent columns it already holds (V is the latent part of the row).
+//     P (bf16) overwrites the score buffer in TMEM and is the A operand of P.V.
 // Each CTA therefore reads 576 of the 1152 bytes of every selected row, once.
 // TMEM per CTA: O [128 heads x 256] fp32 (cols 0-255), q latent part (256-383,
-// bf16 pairs), two score buffers of 64 rows (384-511).
+// bf16 pairs), two score / probability buffers of 64 rows (384-511).
 //
-// Warp roles (192 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
-// TMEM lanes 32w..32w+31 = heads 32w..32w+31), warp 4 index resolution + TMA
-// gathers, warp 5 tcgen05 MMA issue.  Every wait is bounded; a wait that gives up
-// records SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
+// Warp roles (320 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
+// TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, one lane
+// each), warp 8 issues QK^T, warp 9 issues P.V.  Every wait is bounded; a wait that
+// gives up records SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
 #include <cuda.h>
 #include <mutex>
 
@@ -36,7 +37,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kNt = 64;          // selected rows per tile
-constexpr int kStages = 3;       // gather pipeline depth
+constexpr int kStages = 4;       // gather pipeline depth
 constexpr int kHeads = 128;      // heads per unit (padded)
 constexpr int kThreads = 320;
 constexpr int kWarps = kThreads / 32;
@@ -54,26 +55,19 @@ constexpr int kRopeBlk = kNt * 64;                      // the 32-column SW64 ro
 constexpr int kStageBytes = 4 * kLatBlk + kRopeBlk;     // 36 KB
 constexpr int kOffQRope = kStages * kStageBytes;
 constexpr int kQRopeBytes = kHeads * 64;
-constexpr int kOffP = kOffQRope + kQRopeBytes;
-constexpr int kPBytes = kHeads * kNt * 2;               // P [128 heads x 64 rows] bf16, SW128 K-major
-constexpr int kPHalf = kPBytes / 2;                     // the 64 rows one CTA owns
-constexpr int kOffX = kOffP + 2 * kPBytes;
-constexpr int kXBytes = 64 * kNt * 4;                   // partial scores [64 heads x 64 rows] fp32
-constexpr int kOffXStage = kOffX + 2 * kXBytes;
-constexpr int kOffAlpha = kOffXStage + kXBytes;
-constexpr int kOffFin = kOffAlpha + 2 * kHeads * 4;
-constexpr int kOffList = kOffFin + kHeads * 4;
-constexpr int kListCap = 7104;                          // resolved rows kept at once (multiple of kNt)
+constexpr int kOffX = kOffQRope + kQRopeBytes;
+constexpr int kXBytes = kHeads * kNt * 4;               // partial scores [128 heads x 64 rows] fp32
+constexpr int kXWarpBytes = kXBytes / 4;                // the 32 heads of one warp
+constexpr int kOffXStage = kOffX + kXBytes;
+constexpr int kOffList = kOffXStage + kXBytes;
+constexpr int kListCap = 2048;                          // resolved rows kept at once (multiple of kNt)
 constexpr int kOffBar = kOffList + kListCap * 4;
 // barriers
 constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = kBarKvEmpty + kStages,
-              kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2, kBarXFull = kBarSFree + 2,
-              kBarPReady = kBarXFull + 2,
-              kBarPFull = kBarPReady + 2, kBarPFree = kBarPFull + 2, kBarOReady = kBarPFree + 2,
-              kBarXStaged = kBarOReady + 2, kBarXStageFree = kBarXStaged + 1, kBarPvDone = kBarXStageFree + 1,
-              kBarFinLocal = kBarPvDone + 1, kBarFin = kBarFinLocal + 1, kBarMmaFin = kBarFin + 1,
-              kBarMmaFin2 = kBarMmaFin + 1, kBarPvFinal = kBarMmaFin2 + 1,
-              kNumBars = kBarPvFinal + 1;
+              kBarSFull = kBarQReady + 1, kBarSpFree = kBarSFull + 2, kBarOReady = kBarSpFree + 2,
+              kBarXFull = kBarOReady + 2, kBarXFree = kBarXFull + 1, kBarPvDone = kBarXFree + 1,
+              kBarPvFinal = kBarPvDone + 1, kBarMmaFin = kBarPvFinal + 1, kBarMmaFin2 = kBarMmaFin + 1,
+              kNumBars = kBarMmaFin2 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -133,14 +127,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   int* list_s = reinterpret_cast<int*>(smem + kOffList);
-  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
-  float* fin_s = reinterpret_cast<float*>(smem + kOffFin);
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 8);   // [kWarps]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();   // which half of the columns / heads
+  const uint32_t crank = cluster_ctarank();   // which half of the columns
   const uint32_t peer = crank ^ 1u;
   const int unit = blockIdx.x >> 1;
   const int T = p.B * p.Q;
@@ -161,22 +153,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars[kBarQReady], 128);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars[kBarSFull + x], 1);
-      mbar_init(&bars[kBarSFree + x], 128);
-      mbar_init(&bars[kBarXFull + x], 1);    // receiver's arming arrival + the peer's bytes
-      mbar_init(&bars[kBarPReady + x], 64);  // local owners wrote their P rows
-      mbar_init(&bars[kBarPFull + x], 1);    // local owners' arming arrival + the peer's P bytes
-      mbar_init(&bars[kBarPFree + x], 2);    // P.V of this tile done in both CTAs
-      mbar_init(&bars[kBarOReady + x], 128);
+      mbar_init(&bars[kBarSFull + x], 1);     // QK^T of the tile in this score buffer done
+      mbar_init(&bars[kBarSpFree + x], 1);    // P.V reading this buffer's probabilities done
+      mbar_init(&bars[kBarOReady + x], 128);  // probabilities in TMEM and O rescaled
     }
-    mbar_init(&bars[kBarXStaged], 64);
-    mbar_init(&bars[kBarXStageFree], 1);
+    mbar_init(&bars[kBarXFull], 1);           // arming arrival + the peer's 4 x 8 KB of partials
+    mbar_init(&bars[kBarXFree], 4);           // the peer's 4 softmax warps read our partials
     mbar_init(&bars[kBarPvDone], 1);
-    mbar_init(&bars[kBarFinLocal], 64);
-    mbar_init(&bars[kBarFin], 1);
+    mbar_init(&bars[kBarPvFinal], 1);         // the last P.V of the unit has completed
     mbar_init(&bars[kBarMmaFin], 1);
     mbar_init(&bars[kBarMmaFin2], 1);
-    mbar_init(&bars[kBarPvFinal], 1);   // the last P.V of the unit has completed
     *abort_s = 0;
     fence_barrier_init();
   }
@@ -239,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     off += __popc(mask);
   }
   tc_fence_before();
-  cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  cluster_sync();  // both CTAs' barriers are initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
   const int n_tiles = (total + kNt - 1) / kNt;
@@ -261,8 +247,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     // =================== softmax / rescale / epilogue warps =====================
     const int head = warp * 32 + lane;
-    const bool owner = (warp >> 1) == (int)crank;
-    const bool elected = lane == 0 && (warp & 1) == 0;   // first lane of the first warp of a pair
     const bool head_ok = head < p.h;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 
@@ -291,32 +275,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const float c_scale = p.scale * kLog2e;
     const float c_abs = fabsf(c_scale);
-    const int hl = head - 64 * (int)(owner ? crank : peer);  // row of this head in an X buffer
-    char* xbase = smem + kOffX;
-    char* xstage = smem + kOffXStage;
-    char* pbase = smem + kOffP;
+    char* xin = smem + kOffX + head * 256;        // the peer's partial scores of this head
+    char* xout = smem + kOffXStage + head * 256;  // our partial scores of this head, outgoing
+    char* xout_warp = smem + kOffXStage + warp * kXWarpBytes;
+    const uint32_t xdst_warp = mapa(smem + kOffX + warp * kXWarpBytes, peer);
+    const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
+    const uint32_t xfree_peer = mapa(&bars[kBarXFree], peer);
 
-    // rescale this warp's O rows by alpha (any lane != 1) once P.V of tile `prev` is done
-    auto rescale = [&](float alpha, int prev) -> bool {
-      if (!__any_sync(0xffffffffu, alpha != 1.f)) return true;
-      if (!wait_warp(&bars[kBarPvDone], prev & 1)) return false;
+    // Load our partial scores of tile j from TMEM, stage them, and send this warp's 32
+    // heads to the peer (one 8 KB bulk copy).  The staging rows keep our partials: they
+    // are summed with the peer's when tile j is processed.
+    auto send_partials = [&](int j) -> bool {
+      const int bj = j & 1;
+      if (!wait_warp(&bars[kBarSFull + bj], (j >> 1) & 1)) return false;
       tc_fence_after();
-#pragma unroll 1
-      for (int c16 = 0; c16 < 256 / 16; ++c16) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + kColO + 16 * c16, v);
-        tmem_ld_wait();
+      float sj[kNt];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-        tmem_st16(lane_base + kColO + 16 * c16, v);
+      for (int c4 = 0; c4 < kNt / 16; ++c4) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + kColS + kNt * bj + 16 * c4, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) sj[16 * c4 + k] = __uint_as_float(v[k]);
       }
-      tmem_st_wait();
+      tmem_ld_wait();
+      if (j >= 1 && lane == 0) bulk_wait_read<0>();   // previous copy has left the staging rows
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        *reinterpret_cast<float4*>(xout + ((k ^ (head & 15)) * 16)) =
+            make_float4(sj[4 * k], sj[4 * k + 1], sj[4 * k + 2], sj[4 * k + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      // the peer's X buffer holds tile j-1 until all its warps have read it
+      if (j >= 1 && !wait_warp_cluster(&bars[kBarXFree], (j - 1) & 1)) return false;
+      if (lane == 0) {
+        bulk_copy_s2cluster(xdst_warp, xout_warp, kXWarpBytes, xfull_peer);
+        bulk_commit_group();
+      }
+      __syncwarp();
       return true;
     };
-    auto load_s = [&](int i, float (&s)[kNt]) -> bool {
+
+    float m_ref = -INFINITY, l_sum = 0.f;  // running max (log2 units) and sum of this head
+    if (warp == 0 && lane == 0 && n_tiles > 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+    bool ok = n_tiles == 0 || send_partials(0);
+    if (!ok) fail();
+    for (int i = 0; ok && i < n_tiles && !*abort_s; ++i) {
       const int bb = i & 1;
-      if (!wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) return false;
+      // full scores of tile i = our partials (still in this tile's TMEM buffer) + the
+      // peer's (same fp32 sums in both CTAs); parked back in TMEM while the next tile's
+      // partials go out, so that exchange overlaps this tile's exponentials
+      if (!wait_warp_cluster(&bars[kBarXFull], i & 1)) { fail(); break; }
       tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < kNt / 16; ++c4) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 x = *reinterpret_cast<const float4*>(xin + (((4 * c4 + k) ^ (head & 15)) * 16));
+          v[4 * k] = __float_as_uint(__uint_as_float(v[4 * k]) + x.x);
+          v[4 * k + 1] = __float_as_uint(__uint_as_float(v[4 * k + 1]) + x.y);
+          v[4 * k + 2] = __float_as_uint(__uint_as_float(v[4 * k + 2]) + x.z);
+          v[4 * k + 3] = __float_as_uint(__uint_as_float(v[4 * k + 3]) + x.w);
+        }
+        tmem_st16(lane_base + kColS + kNt * bb + 16 * c4, v);
+      }
+      // our reads of the peer's partials are complete (their values are summed): a
+      // relaxed arrive tells the peer it may overwrite the buffer with the next tile
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer);
+      // the next tile's partials go out now if its scores are ready (the exchange then
+      // overlaps this tile's exponentials), else right after this tile's softmax: never
+      // wait for QK^T of tile i+1 here, which itself waits for P.V of tile i-1
+      bool sent = i + 1 >= n_tiles;
+      if (!sent && __all_sync(0xffffffffu, mbar_test(&bars[kBarSFull + (bb ^ 1)], ((i + 1) >> 1) & 1))) {
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+        if (!send_partials(i + 1)) { fail(); break; }
+        sent = true;
+      }
+      tmem_st_wait();
+      float s[kNt];
 #pragma unroll
       for (int c4 = 0; c4 < kNt / 16; ++c4) {
         uint32_t v[16];
@@ -325,195 +365,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 16; ++k) s[16 * c4 + k] = __uint_as_float(v[k]);
       }
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[kBarSFree + bb]);
-      return true;
-    };
-
-    float m_ref = -INFINITY, l_sum = 0.f;  // owner's running max (log2 units) and sum
-    if (owner) {
-      for (int i = 0; i < n_tiles && !*abort_s; ++i) {
-        const int bb = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (elected) mbar_arrive_expect_tx(&bars[kBarXFull + bb], kXBytes);   // arm for the peer's bytes
-        __syncwarp();
-        float s[kNt];
-        if (!load_s(i, s)) { fail(); break; }
-        if (!wait_warp_cluster(&bars[kBarXFull + bb], ph)) { fail(); break; }
-        const char* xr = xbase + bb * kXBytes + hl * 256;
+      // online softmax in log2 units; the reference max only moves when it grows past
+      // the threshold, so O is rarely rescaled
+      const int nvalid = min(kNt, total - kNt * i);
+      if (c_scale < 0.f) {   // keep max(s) * |c| == max(s * c) for a negative scale
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float4 v = *reinterpret_cast<const float4*>(xr + ((k ^ (hl & 15)) * 16));
-          s[4 * k] += v.x;
-          s[4 * k + 1] += v.y;
-          s[4 * k + 2] += v.z;
-          s[4 * k + 3] += v.w;
-        }
-        // online softmax in log2 units; the reference max only moves when it grows past
-        // the threshold, so O is rarely rescaled
-        const int nvalid = min(kNt, total - kNt * i);
-        if (c_scale < 0.f) {   // keep max(s) * |c| == max(s * c) for a negative scale
-#pragma unroll
-          for (int j = 0; j < kNt; ++j) s[j] = -s[j];
-        }
-        if (nvalid < kNt) {
-#pragma unroll
-          for (int j = 0; j < kNt; ++j)
-            if (j >= nvalid) s[j] = -INFINITY;
-        }
-        float mx[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(s[4 * j], s[4 * j + 1]), fmaxf(s[4 * j + 2], s[4 * j + 3]));
-#pragma unroll
-        for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-          for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
-        const float mt = mx[0] * c_abs;
-        float m_new = m_ref;
-        if (i == 0 || mt > m_ref + kRescaleThreshold) m_new = fmaxf(mt, m_ref);
-        const float alpha = i == 0 ? 1.f : ex2(m_ref - m_new);
-        m_ref = m_new;
-        uint32_t pk[kNt / 2];
-        float sm[16];
-#pragma unroll
-        for (int j = 0; j < kNt / 2; ++j) {
-          const float e0 = ex2(fmaf(s[2 * j], c_abs, -m_new));
-          const float e1 = ex2(fmaf(s[2 * j + 1], c_abs, -m_new));
-          if (j < 16) sm[j] = e0 + e1; else sm[j - 16] += e0 + e1;
-          pk[j] = pack_bf16(e0, e1);
-        }
-#pragma unroll
-        for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-          for (int j = 0; j < w2; ++j) sm[j] += sm[j + w2];
-        const float rs = sm[0];
-        l_sum = l_sum * alpha + rs;
-        if (i >= 2 && !wait_warp_cluster(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); break; }
-        char* prow = pbase + bb * kPBytes + head * 128;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(prow + ((k ^ (head & 7)) * 16)) =
-              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        alpha_s[bb * kHeads + head] = alpha;
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[kBarPReady + bb]);
-        if (elected) {
-          // our 64 P rows and alphas -> the peer; our own P.V waits for the peer's half
-          if (!mbar_wait(&bars[kBarPReady + bb], ph, wl)) {
-            fail();
-          } else {
-            mbar_arrive_expect_tx(&bars[kBarPFull + bb], kPHalf + 64 * 4);
-            const uint32_t rbar = mapa(&bars[kBarPFull + bb], peer);
-            char* psrc = pbase + bb * kPBytes + kPHalf * crank;
-            bulk_copy_s2cluster(mapa(psrc, peer), psrc, kPHalf, rbar);
-            float* asrc = alpha_s + bb * kHeads + 64 * crank;
-            bulk_copy_s2cluster(mapa(asrc, peer), asrc, 64 * 4, rbar);
-            bulk_commit_group();
-          }
-        }
-        __syncwarp();
-        if (i >= 1 && !rescale(alpha, i - 1)) { fail(); break; }
-        tc_fence_before();
-        mbar_arrive(&bars[kBarOReady + bb]);
+        for (int j = 0; j < kNt; ++j) s[j] = -s[j];
       }
-    } else {
-      // sender warps: two streams of work, handled in whichever order they become ready:
-      //   send(ns):   partial scores of the peer's heads for tile ns -> the peer's X buffer
-      //   finish(nf): once the peer's P / alpha of tile nf landed, rescale these heads' O
-      //               rows if their reference max moved, and release P.V of tile nf
-      // (finishing never waits behind a late gather of a later tile)
-      int ns = 0, nf = 0;
-      long long idle = 0;
-      const uint64_t t_start = globaltimer_ns();
-      while (nf < n_tiles && !*abort_s) {
-        bool progressed = false;
-        if (ns < n_tiles && ns <= nf + 1 &&
-            __all_sync(0xffffffffu, mbar_test(&bars[kBarSFull + (ns & 1)], (ns >> 1) & 1))) {
-          const int i = ns, bb = i & 1;
-          float s[kNt];
-          if (!load_s(i, s)) { fail(); break; }
-          if (i >= 1 && !wait_warp(&bars[kBarXStageFree], (i - 1) & 1)) { fail(); break; }
-          char* xr = xstage + hl * 256;
+      if (nvalid < kNt) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            *reinterpret_cast<float4*>(xr + ((k ^ (hl & 15)) * 16)) =
-                make_float4(s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3]);
-          fence_proxy_async_smem();
-          mbar_arrive(&bars[kBarXStaged]);
-          if (elected) {
-            bool ok = mbar_wait(&bars[kBarXStaged], i & 1, wl);
-            // the peer's X buffer bb was read by the peer's owners for tile i-2 before
-            // they sent us their P of that tile: P(i-2) landing here frees the buffer
-            ok = ok && (i < 2 || mbar_wait<true>(&bars[kBarPFull + bb], ((i >> 1) - 1) & 1, wl));
-            if (!ok) {
-              fail();
-            } else {
-              bulk_copy_s2cluster(mapa(xbase + bb * kXBytes, peer), xstage, kXBytes,
-                                  mapa(&bars[kBarXFull + bb], peer));
-              bulk_commit_group();
-              bulk_wait_read<0>();
-              mbar_arrive(&bars[kBarXStageFree]);
-            }
-          }
-          __syncwarp();
-          ++ns;
-          progressed = true;
+        for (int j = 0; j < kNt; ++j)
+          if (j >= nvalid) s[j] = -INFINITY;
+      }
+      float mx[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) mx[j] = fmaxf(fmaxf(s[4 * j], s[4 * j + 1]), fmaxf(s[4 * j + 2], s[4 * j + 3]));
+#pragma unroll
+      for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+        for (int j = 0; j < w2; ++j) mx[j] = fmaxf(mx[j], mx[j + w2]);
+      const float mt = mx[0] * c_abs;
+      float m_new = m_ref;
+      if (i == 0 || mt > m_ref + kRescaleThreshold) m_new = fmaxf(mt, m_ref);
+      const float alpha = i == 0 ? 1.f : ex2(m_ref - m_new);
+      m_ref = m_new;
+      uint32_t pk[kNt / 2];
+      float sm[16];
+#pragma unroll
+      for (int j = 0; j < kNt / 2; ++j) {
+        const float e0 = ex2(fmaf(s[2 * j], c_abs, -m_new));
+        const float e1 = ex2(fmaf(s[2 * j + 1], c_abs, -m_new));
+        if (j < 16) sm[j] = e0 + e1; else sm[j - 16] += e0 + e1;
+        pk[j] = pack_bf16(e0, e1);
+      }
+#pragma unroll
+      for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+        for (int j = 0; j < w2; ++j) sm[j] += sm[j + w2];
+      l_sum = l_sum * alpha + sm[0];
+      // probabilities (bf16 pairs) overwrite the first 32 columns of this tile's score
+      // buffer (its scores were read when the tile's partials were sent)
+      {
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = pk[k];
+        tmem_st16(lane_base + kColS + kNt * bb, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = pk[16 + k];
+        tmem_st16(lane_base + kColS + kNt * bb + 16, v);
+      }
+      // rescale this warp's O rows if any of its heads' reference max moved (P.V of
+      // the previous tile must be complete first)
+      if (i >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!wait_warp(&bars[kBarPvDone], (i - 1) & 1)) { fail(); break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c16 = 0; c16 < 256 / 16; ++c16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + kColO + 16 * c16, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+          tmem_st16(lane_base + kColO + 16 * c16, v);
         }
-        if (nf < ns && __all_sync(0xffffffffu, mbar_test_cluster(&bars[kBarPFull + (nf & 1)], (nf >> 1) & 1))) {
-          const int pb = nf & 1;
-          const float alpha = alpha_s[pb * kHeads + head];
-          if (nf >= 1 && !rescale(alpha, nf - 1)) { fail(); break; }
-          tc_fence_before();
-          mbar_arrive(&bars[kBarOReady + pb]);
-          ++nf;
-          progressed = true;
-        }
-        if (!progressed) {
-          if (++idle >= wl || ((idle & 1023) == 0 && globaltimer_ns() - t_start > 4000000000ull)) { fail(); break; }
-          __nanosleep(20);
-        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[kBarOReady + bb]);
+      if (!sent) {
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+        if (!send_partials(i + 1)) { fail(); break; }
       }
     }
+    if (lane == 0) bulk_wait<0>();   // every copy this warp issued has landed
+    __syncwarp();
 
-    // ---- epilogue: out = O / l for this CTA's 256 columns, lse by the owner ----
+    // ---- epilogue: out = O / l for this CTA's 256 columns; lse from CTA 0 --------
     float* out = p.out + ((size_t)r * T + t) * p.h * kDV + 256 * crank;
     float* lse = p.lse + ((size_t)r * T + t) * p.h;
     if (n_tiles == 0) {
       if (head_ok) {
         float4* o4 = reinterpret_cast<float4*>(out + (size_t)head * kDV);
         for (int k = 0; k < 64; ++k) o4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (owner) lse[head] = -INFINITY;
+        if (crank == 0) lse[head] = -INFINITY;
       }
     } else if (!*abort_s) {
-      bool ok = true;
-      float l_head = l_sum;
-      if (owner) {
-        fin_s[head] = l_sum;
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[kBarFinLocal]);
-        if (elected) {
-          if (!mbar_wait(&bars[kBarFinLocal], 0, wl)) {
-            fail();
-          } else {
-            bulk_copy_s2cluster(mapa(fin_s + 64 * crank, peer), fin_s + 64 * crank, 64 * 4,
-                                mapa(&bars[kBarFin], peer));
-            bulk_commit_group();
-          }
-        }
-        __syncwarp();
-      } else {
-        if (elected) mbar_arrive_expect_tx(&bars[kBarFin], 64 * 4);
-        __syncwarp();
-        ok = wait_warp_cluster(&bars[kBarFin], 0);
-        l_head = fin_s[head];
-      }
       // a dedicated one-phase barrier: pv_done may still be two phases behind here
-      ok = wait_warp(&bars[kBarPvFinal], 0) && ok;
-      if (!ok) {
+      if (!wait_warp(&bars[kBarPvFinal], 0)) {
         fail();
       } else {
         tc_fence_after();
-        const float inv = 1.f / l_head;
+        const float inv = 1.f / l_sum;
         float4* o4 = reinterpret_cast<float4*>(out + (size_t)head * kDV);
 #pragma unroll 1
         for (int c16 = 0; c16 < 256 / 16; ++c16) {
@@ -527,11 +469,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                             __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
           }
         }
-        if (owner && head_ok) lse[head] = (m_ref + __log2f(l_head)) * kLn2;
+        if (crank == 0 && head_ok) lse[head] = (m_ref + __log2f(l_sum)) * kLn2;
       }
     }
-    if (elected) bulk_wait<0>();   // every copy this thread issued has landed
-    __syncwarp();
   } else if (warp < kProducerWarp + kProducerWarps) {
     // =================== gathers ===================================================
     // Producer warp pw issues, from one lane, the gathers of row groups g = pw, pw+4,
@@ -587,9 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
         report_status(p.status, kStatusTimeout);
   } else if (warp == kMmaWarp || warp == kPvWarp) {
-    // =================== tcgen05 MMA issue: QK^T (warp 5) and P.V (warp 6) ========
-    // Two issuing threads, so that QK^T of later tiles never waits behind a P.V that
-    // is still waiting for its probabilities.
+    // =================== tcgen05 MMA issue: QK^T (warp 8) and P.V (warp 9) ========
     if (lane == 0 && n_tiles > 0) {
       bool ok = true;
       if (warp == kMmaWarp) {
@@ -600,7 +538,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
           const int s = n % kStages, bb = n & 1;
           if (!(ok = mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl))) break;
-          if (n >= 2 && !(ok = mbar_wait(&bars[kBarSFree + bb], ((n >> 1) - 1) & 1, wl))) break;
+          // the score buffer is free once P.V of tile n-2 has read its probabilities
+          if (n >= 2 && !(ok = mbar_wait(&bars[kBarSpFree + bb], ((n >> 1) - 1) & 1, wl))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * kStageBytes);
           const uint32_t d = tmem + kColS + kNt * bb;
@@ -618,18 +557,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
         for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
           const int s = n % kStages, bb = n & 1;
-          if (!(ok = mbar_wait<true>(&bars[kBarPFull + bb], (n >> 1) & 1, wl))) break;
           if (!(ok = mbar_wait(&bars[kBarOReady + bb], (n >> 1) & 1, wl))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * kStageBytes);
-          const uint32_t pa = smem_u32(smem + kOffP + bb * kPBytes);
 #pragma unroll
           for (int k = 0; k < kNt / 16; ++k)
-            mma_ss(tmem + kColO, smem_desc(pa + 32 * k, 16, 1024, kSwizzle128),
+            mma_ts(tmem + kColO, tmem + kColS + kNt * bb + 8 * k,
                    smem_desc(st + 2048 * k, kLatBlk, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bars[kBarKvEmpty + s]);
+          mma_commit(&bars[kBarSpFree + bb]);
           mma_commit(&bars[kBarPvDone]);
-          mma_commit_mc(&bars[kBarPFree + bb], 0x3);
           if (n == n_tiles - 1) mma_commit(&bars[kBarPvFinal]);
         }
       }
