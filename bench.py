@@ -14,6 +14,7 @@ reported time is the max over ranks and `value` aggregates all ranks' work.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -145,12 +146,25 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the slowest rank's time sets the job's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_workload(w: workloads.Workload, rank: int) -> workloads.Workload:
+    """The batch rank `rank` decodes: the same shapes as `w`, its own tokens (seed
+    offset by the rank), so N ranks process N independent batches (weak scaling)."""
+    return dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
+
+
+def job_value(flops_per_rank: float, ms: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's step time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 def cpu_oracle_leg(inp, acc, target_s=15.0, max_tokens=None):
@@ -223,7 +237,7 @@ def run_reference(args, world, rank):
 
 def run_ours(args, world, rank, local):
     import deepseek_sparse_mla_sfa_gb300 as sfa
-    w = workloads.CONFIGS[args.config]
+    w = rank_workload(workloads.CONFIGS[args.config], rank)
     peaks = load_peaks()
     inp = workloads.make(w, device="cuda")
     acc = accounting(inp)
@@ -285,7 +299,7 @@ def run_ours(args, world, rank, local):
     dec_avg = sum(dec_ms) / max(1, len(dec_ms))
     mrg_avg = sum(mrg_ms) / max(1, len(mrg_ms))
 
-    value = world * acc["flops"] / (ms * 1e-3) / 1e12
+    value = job_value(acc["flops"], ms, world)
     gather_gbs = acc["gather_bytes"] / (ms * 1e-3) / 1e9
     alg_gbs = acc["total_bytes"] / (ms * 1e-3) / 1e9
     roof_s = max(acc["flops"] / (peaks["bf16_tflops"] * 1e12), acc["total_bytes"] / (peaks["hbm_gbs"] * 1e9))
@@ -393,7 +407,6 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.batch:
-        import dataclasses
         w = dataclasses.replace(workloads.CONFIGS[args.config], B=args.batch,
                                 name=f"{args.config}_b{args.batch}")
         workloads.CONFIGS[w.name] = w

@@ -19,7 +19,10 @@
 //     P (bf16) overwrites the score buffer in TMEM and is the A operand of P.V.
 // Each CTA therefore reads 576 of the 1152 bytes of every selected row, once.
 // TMEM per CTA: O [128 heads x 256] fp32 (cols 0-255), q latent part (256-383,
-// bf16 pairs), two score / probability buffers of 64 rows (384-511).
+// bf16 pairs), two score / probability buffers of 64 rows (384-511).  q arrives by
+// TMA at kernel start: its latent half lands in the (still idle) score-exchange
+// buffers, from where the softmax warps move it into TMEM, and its rope part lands
+// in place as the shared-memory operand of the rope columns of QK^T.
 //
 // Warp roles (320 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
 // TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, one lane
@@ -59,6 +62,8 @@ constexpr int kOffX = kOffQRope + kQRopeBytes;
 constexpr int kXBytes = kHeads * kNt * 4;               // partial scores [128 heads x 64 rows] fp32
 constexpr int kXWarpBytes = kXBytes / 4;                // the 32 heads of one warp
 constexpr int kOffXStage = kOffX + kXBytes;
+constexpr int kQBox = kHeads * 128;                     // one 64-column SW128 box of q's latent half
+static_assert(4 * kQBox == 2 * kXBytes, "q's latent half fills the two exchange buffers");
 constexpr int kOffList = kOffXStage + kXBytes;
 constexpr int kListCap = 2048;                          // resolved rows kept at once (multiple of kNt)
 constexpr int kOffBar = kOffList + kListCap * 4;
@@ -67,7 +72,7 @@ constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = k
               kBarSFull = kBarQReady + 1, kBarSpFree = kBarSFull + 2, kBarOReady = kBarSpFree + 2,
               kBarXFull = kBarOReady + 2, kBarXFree = kBarXFull + 1, kBarPvDone = kBarXFree + 1,
               kBarPvFinal = kBarPvDone + 1, kBarMmaFin = kBarPvFinal + 1, kBarMmaFin2 = kBarMmaFin + 1,
-              kNumBars = kBarMmaFin2 + 1;
+              kBarQLoad = kBarMmaFin2 + 1, kNumBars = kBarQLoad + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;         // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -85,6 +90,7 @@ constexpr uint32_t kStageTx = kStageBytes;  // bytes a full tile delivers (OOB r
 struct TcParams {
   DecodeParams p;
   int num_rows;  // num_blocks * block_size (== out-of-range row used for padding)
+  int q_rows;    // heads per q box: min(h, 128)
 };
 
 __device__ __forceinline__ int lanemask_lt() {
@@ -121,7 +127,9 @@ __device__ __forceinline__ int resolve_row(const DecodeParams& p, int b, int pos
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_lat,
-                     const __grid_constant__ CUtensorMap tmap_rope, const TcParams tp) {
+                     const __grid_constant__ CUtensorMap tmap_rope,
+                     const __grid_constant__ CUtensorMap tmap_qlat,
+                     const __grid_constant__ CUtensorMap tmap_qrope, const TcParams tp) {
   const DecodeParams& p = tp.p;
   extern __shared__ char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,13 +166,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarOReady + x], 128);  // probabilities in TMEM and O rescaled
     }
     mbar_init(&bars[kBarXFull], 1);           // arming arrival + the peer's 4 x 8 KB of partials
-    mbar_init(&bars[kBarXFree], 4);           // the peer's 4 softmax warps read our partials
+    mbar_init(&bars[kBarXFree], 4);           // the peer's 4 softmax warps read our partials (phase
+                                              // 0: they have moved their q out of their buffers)
     mbar_init(&bars[kBarPvDone], 1);
     mbar_init(&bars[kBarPvFinal], 1);         // the last P.V of the unit has completed
     mbar_init(&bars[kBarMmaFin], 1);
     mbar_init(&bars[kBarMmaFin2], 1);
+    mbar_init(&bars[kBarQLoad], 1);
     *abort_s = 0;
     fence_barrier_init();
+    // q of this token: latent columns [256c, 256c+256) as four SW128 boxes into the
+    // exchange buffers, rope columns [512+32c, +32) as one SW64 box into qrope
+    mbar_arrive_expect_tx(&bars[kBarQLoad], (uint32_t)(tp.q_rows * (4 * 128 + 64)));
+    for (int j = 0; j < 4; ++j)
+      tma_load_3d(smem_u32(smem + kOffX + j * kQBox), &tmap_qlat, 256 * crank + 64 * j, 0, t, &bars[kBarQLoad]);
+    tma_load_3d(smem_u32(smem + kOffQRope), &tmap_qrope, 512 + 32 * crank, 0, t, &bars[kBarQLoad]);
   }
   if (warp == 0) {
     tmem_alloc(tmem_base_s, kTmemCols);
@@ -250,26 +266,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool head_ok = head < p.h;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 
-    // q: latent columns [256c, 256c+256) -> TMEM (bf16 pairs), rope [512+32c, +32) -> smem
+    const uint32_t xfree_peer = mapa(&bars[kBarXFree], peer);
+    // q's latent half: from the SW128 boxes in the exchange buffers into TMEM (bf16
+    // pairs); every softmax warp is done with those buffers before any of them reuses
+    // its slice, and the peer may write into ours once all four warps have arrived
     {
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          p.q + ((size_t)t * p.h + (head_ok ? head : 0)) * kDQK);
+      bool qok = wait_warp(&bars[kBarQLoad], 0);
+      if (!qok) fail();
+      const bool have = qok && head < tp.q_rows;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t v[16];
+      for (int j = 0; j < 4; ++j) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = head_ok ? __ldg(qrow + 128 * crank + 16 * j + k) : 0u;
-        tmem_st16(lane_base + kColQ + 16 * j, v);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int ch = 4 * hh + c;
+            const uint4 x = have ? *reinterpret_cast<const uint4*>(smem + kOffX + j * kQBox + head * 128 +
+                                                                   ((ch ^ (head & 7)) * 16))
+                                 : make_uint4(0, 0, 0, 0);
+            v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+          }
+          tmem_st16(lane_base + kColQ + 32 * j + 16 * hh, v);
+        }
       }
-      const uint4* qr = reinterpret_cast<const uint4*>(qrow + 256 + 16 * crank);
+      if (head >= tp.q_rows) {   // heads past h: zero rope row (the box stops at h)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint4 v = head_ok ? __ldg(qr + k) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qrope + head * 64 + ((k ^ ((head >> 1) & 3)) * 16)) = v;
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(qrope + head * 64 + ((k ^ ((head >> 1) & 3)) * 16)) = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
+      named_barrier(1, 128);
+      if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer);
       mbar_arrive(&bars[kBarQReady]);
     }
 
@@ -280,7 +310,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     char* xout_warp = smem + kOffXStage + warp * kXWarpBytes;
     const uint32_t xdst_warp = mapa(smem + kOffX + warp * kXWarpBytes, peer);
     const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
-    const uint32_t xfree_peer = mapa(&bars[kBarXFree], peer);
 
     // Load our partial scores of tile j from TMEM, stage them, and send this warp's 32
     // heads to the peer (one 8 KB bulk copy).  The staging rows keep our partials: they
@@ -306,8 +335,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             make_float4(sj[4 * k], sj[4 * k + 1], sj[4 * k + 2], sj[4 * k + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      // the peer's X buffer holds tile j-1 until all its warps have read it
-      if (j >= 1 && !wait_warp_cluster(&bars[kBarXFree], (j - 1) & 1)) return false;
+      // the peer's X buffer holds its q (j = 0) or tile j-1 until all its warps have read it
+      if (!wait_warp_cluster(&bars[kBarXFree], j & 1)) return false;
       if (lane == 0) {
         bulk_copy_s2cluster(xdst_warp, xout_warp, kXWarpBytes, xfull_peer);
         bulk_commit_group();
@@ -605,6 +634,20 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// q [T, h, 576] as a 3D tensor (columns, heads, tokens); one box = box_cols columns of
+// q_rows heads of one token
+bool make_q_map(CUtensorMap* m, const void* q, int h, long long T, int q_rows, int box_cols, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)h, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)h * kDQK * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)q_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_row_map(CUtensorMap* m, const void* kv, int num_rows, int box_cols, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -622,6 +665,11 @@ bool make_row_map(CUtensorMap* m, const void* kv, int num_rows, int box_cols, CU
 bool tc_supports(int h, int block_size) {
   (void)block_size;
   return h >= 1 && h <= kHeads;
+}
+
+bool tc_supports_ptrs(const void* q, const void* kv) {
+  // tensor maps want 16-byte aligned base addresses
+  return (reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(kv) & 15) == 0;
 }
 
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits) {
@@ -643,9 +691,12 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   TcParams tp;
   tp.p = p;
   tp.num_rows = (int)num_rows;
-  CUtensorMap lat, rope;
+  tp.q_rows = p.h < kHeads ? p.h : kHeads;
+  CUtensorMap lat, rope, qlat, qrope;
   if (!make_row_map(&lat, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_row_map(&rope, p.kv, (int)num_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_row_map(&rope, p.kv, (int)num_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_q_map(&qlat, p.q, p.h, T, tp.q_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_q_map(&qrope, p.q, p.h, T, tp.q_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -655,7 +706,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, tp);
+  decode_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, qlat, qrope, tp);
   return cudaGetLastError();
 }
 
