@@ -24,10 +24,12 @@
 // buffers, from where the softmax warps move it into TMEM, and its rope part lands
 // in place as the shared-memory operand of the rope columns of QK^T.
 //
-// Warp roles (320 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
+// Warp roles (448 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
 // TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, one lane
-// each), warp 8 issues QK^T, warp 9 issues P.V.  Every wait is bounded; a wait that
-// gives up records SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
+// each), warp 8 issues QK^T, warp 9 issues P.V, warps 10-13 send each tile's
+// partial scores to the peer as soon as QK^T has produced them (warp w serves TMEM
+// lane quadrant w % 4).  Every wait is bounded; a wait that gives up records
+// SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
 #include <cuda.h>
 #include <mutex>
 
@@ -42,12 +44,13 @@ using namespace ptx;
 constexpr int kNt = 64;          // selected rows per tile
 constexpr int kStages = 4;       // gather pipeline depth
 constexpr int kHeads = 128;      // heads per unit (padded)
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kWarps = kThreads / 32;
 constexpr int kProducerWarp = 4;  // warps 4..7 issue the gathers (one lane each)
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = 8;        // issues QK^T
 constexpr int kPvWarp = 9;         // issues P.V
+constexpr int kSendWarp = 10;      // warps 10..13 send partial scores
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P entries stay below 2^8
@@ -72,9 +75,10 @@ constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = k
               kBarSFull = kBarQReady + 1, kBarSpFree = kBarSFull + 2, kBarOReady = kBarSpFree + 2,
               kBarXFull = kBarOReady + 2, kBarXFree = kBarXFull + 1, kBarPvDone = kBarXFree + 1,
               kBarPvFinal = kBarPvDone + 1, kBarMmaFin = kBarPvFinal + 1, kBarMmaFin2 = kBarMmaFin + 1,
-              kBarQLoad = kBarMmaFin2 + 1, kNumBars = kBarQLoad + 1;
+              kBarQLoad = kBarMmaFin2 + 1, kBarSRead = kBarQLoad + 1, kNumBars = kBarSRead + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;         // + alignment slack
+constexpr int kSmemBytes = kOffMisc + 128 + 1024;        // + alignment slack
+static_assert(8 + 4 * kWarps <= 128, "misc area");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kStageBytes % 1024 == 0, "stages must stay 1024-byte aligned");
 static_assert(kListCap % kNt == 0, "list segments hold whole tiles");
@@ -173,6 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarMmaFin], 1);
     mbar_init(&bars[kBarMmaFin2], 1);
     mbar_init(&bars[kBarQLoad], 1);
+    for (int x = 0; x < 2; ++x) mbar_init(&bars[kBarSRead + x], 4);   // senders have read this score buffer
     *abort_s = 0;
     fence_barrier_init();
     // q of this token: latent columns [256c, 256c+256) as four SW128 boxes into the
@@ -305,95 +310,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const float c_scale = p.scale * kLog2e;
     const float c_abs = fabsf(c_scale);
-    char* xin = smem + kOffX + head * 256;        // the peer's partial scores of this head
-    char* xout = smem + kOffXStage + head * 256;  // our partial scores of this head, outgoing
-    char* xout_warp = smem + kOffXStage + warp * kXWarpBytes;
-    const uint32_t xdst_warp = mapa(smem + kOffX + warp * kXWarpBytes, peer);
-    const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
-
-    // Load our partial scores of tile j from TMEM, stage them, and send this warp's 32
-    // heads to the peer (one 8 KB bulk copy).  The staging rows keep our partials: they
-    // are summed with the peer's when tile j is processed.
-    auto send_partials = [&](int j) -> bool {
-      const int bj = j & 1;
-      if (!wait_warp(&bars[kBarSFull + bj], (j >> 1) & 1)) return false;
-      tc_fence_after();
-      float sj[kNt];
-#pragma unroll
-      for (int c4 = 0; c4 < kNt / 16; ++c4) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + kColS + kNt * bj + 16 * c4, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) sj[16 * c4 + k] = __uint_as_float(v[k]);
-      }
-      tmem_ld_wait();
-      if (j >= 1 && lane == 0) bulk_wait_read<0>();   // previous copy has left the staging rows
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        *reinterpret_cast<float4*>(xout + ((k ^ (head & 15)) * 16)) =
-            make_float4(sj[4 * k], sj[4 * k + 1], sj[4 * k + 2], sj[4 * k + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      // the peer's X buffer holds its q (j = 0) or tile j-1 until all its warps have read it
-      if (!wait_warp_cluster(&bars[kBarXFree], j & 1)) return false;
-      if (lane == 0) {
-        bulk_copy_s2cluster(xdst_warp, xout_warp, kXWarpBytes, xfull_peer);
-        bulk_commit_group();
-      }
-      __syncwarp();
-      return true;
-    };
+    const char* xin = smem + kOffX + head * 256;   // the peer's partial scores of this head
 
     float m_ref = -INFINITY, l_sum = 0.f;  // running max (log2 units) and sum of this head
     if (warp == 0 && lane == 0 && n_tiles > 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
-    bool ok = n_tiles == 0 || send_partials(0);
-    if (!ok) fail();
-    for (int i = 0; ok && i < n_tiles && !*abort_s; ++i) {
+    for (int i = 0; i < n_tiles && !*abort_s; ++i) {
       const int bb = i & 1;
-      // full scores of tile i = our partials (still in this tile's TMEM buffer) + the
-      // peer's (same fp32 sums in both CTAs); parked back in TMEM while the next tile's
-      // partials go out, so that exchange overlaps this tile's exponentials
+      // full scores of tile i = our partials (in this tile's TMEM score buffer) + the
+      // peer's (in X); both CTAs form the same fp32 sums
       if (!wait_warp_cluster(&bars[kBarXFull], i & 1)) { fail(); break; }
+      if (warp == 0 && lane == 0 && i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+      if (!wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); break; }
       tc_fence_after();
+      float s[kNt];
+      {
+        uint32_t v[4][16];
 #pragma unroll
-      for (int c4 = 0; c4 < kNt / 16; ++c4) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v);
+        for (int c4 = 0; c4 < kNt / 16; ++c4) tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v[c4]);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 x = *reinterpret_cast<const float4*>(xin + (((4 * c4 + k) ^ (head & 15)) * 16));
-          v[4 * k] = __float_as_uint(__uint_as_float(v[4 * k]) + x.x);
-          v[4 * k + 1] = __float_as_uint(__uint_as_float(v[4 * k + 1]) + x.y);
-          v[4 * k + 2] = __float_as_uint(__uint_as_float(v[4 * k + 2]) + x.z);
-          v[4 * k + 3] = __float_as_uint(__uint_as_float(v[4 * k + 3]) + x.w);
+        for (int k = 0; k < kNt / 4; ++k) {
+          const float4 x = *reinterpret_cast<const float4*>(xin + ((k ^ (head & 15)) * 16));
+          s[4 * k] = __uint_as_float(v[k >> 2][4 * (k & 3)]) + x.x;
+          s[4 * k + 1] = __uint_as_float(v[k >> 2][4 * (k & 3) + 1]) + x.y;
+          s[4 * k + 2] = __uint_as_float(v[k >> 2][4 * (k & 3) + 2]) + x.z;
+          s[4 * k + 3] = __uint_as_float(v[k >> 2][4 * (k & 3) + 3]) + x.w;
         }
-        tmem_st16(lane_base + kColS + kNt * bb + 16 * c4, v);
       }
-      // our reads of the peer's partials are complete (their values are summed): a
-      // relaxed arrive tells the peer it may overwrite the buffer with the next tile
+      // our reads of the peer's partials are complete: a relaxed arrive tells the peer
+      // it may overwrite X with the next tile
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer);
-      // the next tile's partials go out now if its scores are ready (the exchange then
-      // overlaps this tile's exponentials), else right after this tile's softmax: never
-      // wait for QK^T of tile i+1 here, which itself waits for P.V of tile i-1
-      bool sent = i + 1 >= n_tiles;
-      if (!sent && __all_sync(0xffffffffu, mbar_test(&bars[kBarSFull + (bb ^ 1)], ((i + 1) >> 1) & 1))) {
-        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
-        if (!send_partials(i + 1)) { fail(); break; }
-        sent = true;
-      }
-      tmem_st_wait();
-      float s[kNt];
-#pragma unroll
-      for (int c4 = 0; c4 < kNt / 16; ++c4) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) s[16 * c4 + k] = __uint_as_float(v[k]);
-      }
-      tmem_ld_wait();
       // online softmax in log2 units; the reference max only moves when it grows past
       // the threshold, so O is rarely rescaled
       const int nvalid = min(kNt, total - kNt * i);
@@ -433,7 +380,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = 0; j < w2; ++j) sm[j] += sm[j + w2];
       l_sum = l_sum * alpha + sm[0];
       // probabilities (bf16 pairs) overwrite the first 32 columns of this tile's score
-      // buffer (its scores were read when the tile's partials were sent)
+      // buffer, once the sender warps have read our partials out of it
+      if (!wait_warp(&bars[kBarSRead + bb], (i >> 1) & 1)) { fail(); break; }
+      tc_fence_after();
       {
         uint32_t v[16];
 #pragma unroll
@@ -461,13 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kBarOReady + bb]);
-      if (!sent) {
-        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
-        if (!send_partials(i + 1)) { fail(); break; }
-      }
     }
-    if (lane == 0) bulk_wait<0>();   // every copy this warp issued has landed
-    __syncwarp();
 
     // ---- epilogue: out = O / l for this CTA's 256 columns; lse from CTA 0 --------
     float* out = p.out + ((size_t)r * T + t) * p.h * kDV + 256 * crank;
@@ -555,6 +498,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
         report_status(p.status, kStatusTimeout);
+  } else if (warp >= kSendWarp) {
+    // =================== partial-score senders =====================================
+    // Sender warp w serves TMEM lane quadrant w % 4 (heads 32(w%4) .. +31): for every
+    // tile it loads our partial scores from the TMEM score buffer, stages them, and
+    // copies them into the peer's X buffer (one 8 KB bulk copy) as soon as QK^T is done.
+    const int qd = warp & 3;
+    const int head = qd * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+    char* xout = smem + kOffXStage + head * 256;
+    char* xout_warp = smem + kOffXStage + qd * kXWarpBytes;
+    const uint32_t xdst_warp = mapa(smem + kOffX + qd * kXWarpBytes, peer);
+    const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
+    // the staging rows held q until the softmax warps moved it into TMEM
+    bool ok = n_tiles == 0 || wait_warp(&bars[kBarQReady], 0);
+    for (int j = 0; ok && j < n_tiles && !*abort_s; ++j) {
+      const int bj = j & 1;
+      if (!(ok = wait_warp(&bars[kBarSFull + bj], (j >> 1) & 1))) break;
+      tc_fence_after();
+      uint32_t v[4][16];
+#pragma unroll
+      for (int c4 = 0; c4 < kNt / 16; ++c4) tmem_ld16(lane_base + kColS + kNt * bj + 16 * c4, v[c4]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarSRead + bj]);
+      if (j >= 1 && lane == 0) bulk_wait_read<0>();   // previous copy has left the staging rows
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        *reinterpret_cast<uint4*>(xout + ((k ^ (head & 15)) * 16)) =
+            make_uint4(v[k >> 2][4 * (k & 3)], v[k >> 2][4 * (k & 3) + 1], v[k >> 2][4 * (k & 3) + 2],
+                       v[k >> 2][4 * (k & 3) + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      // the peer's X buffer holds its q (j = 0) or tile j-1 until all its warps have read it
+      if (!(ok = wait_warp_cluster(&bars[kBarXFree], j & 1))) break;
+      if (lane == 0) {
+        bulk_copy_s2cluster(xdst_warp, xout_warp, kXWarpBytes, xfull_peer);
+        bulk_commit_group();
+      }
+      __syncwarp();
+    }
+    if (!ok) fail();
+    if (lane == 0) bulk_wait<0>();   // every copy this warp issued has landed
+    __syncwarp();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // =================== tcgen05 MMA issue: QK^T (warp 8) and P.V (warp 9) ========
     if (lane == 0 && n_tiles > 0) {
