@@ -16,13 +16,14 @@
 //     probabilities, running max and sum agree bit for bit without exchanging them;
 //   * P.V is split by output columns: CTA c owns out[:, 256c : 256c+256), which
 //     are the latent columns it already holds (V is the latent part of the row).
-//     P (bf16) overwrites the score buffer in TMEM and is the A operand of P.V.
+//     P (bf16) goes to a shared-memory tile, the A operand of P.V, so a score
+//     buffer is free for the next QK^T as soon as its scores have been read.
 // Each CTA therefore reads 576 of the 1152 bytes of every selected row, once.
 // TMEM per CTA: O [128 heads x 256] fp32 (cols 0-255), q latent part (256-383,
-// bf16 pairs), two score / probability buffers of 64 rows (384-511).  q arrives by
-// TMA at kernel start: its latent half lands in the (still idle) score-exchange
-// buffers, from where the softmax warps move it into TMEM, and its rope part lands
-// in place as the shared-memory operand of the rope columns of QK^T.
+// bf16 pairs), two score buffers of 64 rows (384-511).  q arrives by TMA at kernel
+// start: its latent half lands in the (still idle) exchange and P buffers, from where
+// the softmax warps move it into TMEM, and its rope part lands in place as the
+// shared-memory operand of the rope columns of QK^T.
 //
 // Warp roles (448 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
 // TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, one lane
@@ -64,10 +65,15 @@ constexpr int kQRopeBytes = kHeads * 64;
 constexpr int kOffX = kOffQRope + kQRopeBytes;
 constexpr int kXBytes = kHeads * kNt * 4;               // partial scores [128 heads x 64 rows] fp32
 constexpr int kXWarpBytes = kXBytes / 4;                // the 32 heads of one warp
-constexpr int kOffXStage = kOffX + kXBytes;
+constexpr int kXHalfBytes = kXWarpBytes / 2;            // 16 heads: one staging slot / bulk copy
+constexpr int kOffXStage = kOffX + kXBytes;             // outgoing partials, 16 heads per warp at once
+constexpr int kXStageBytes = 4 * kXHalfBytes;
+constexpr int kOffP = kOffXStage + kXStageBytes;        // P [128 heads x 64 rows] bf16, K-major SW128
+constexpr int kPBytes = kHeads * kNt * 2;
 constexpr int kQBox = kHeads * 128;                     // one 64-column SW128 box of q's latent half
-static_assert(4 * kQBox == 2 * kXBytes, "q's latent half fills the two exchange buffers");
-constexpr int kOffList = kOffXStage + kXBytes;
+static_assert(4 * kQBox == kXBytes + kXStageBytes + kPBytes, "q's latent half fills X, staging and P");
+static_assert(kOffX % 1024 == 0 && kOffP % 1024 == 0, "SW128 operands need 1024-byte alignment");
+constexpr int kOffList = kOffP + kPBytes;
 constexpr int kListCap = 2048;                          // resolved rows kept at once (multiple of kNt)
 constexpr int kOffBar = kOffList + kListCap * 4;
 // barriers
@@ -75,7 +81,7 @@ constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = k
               kBarSFull = kBarQReady + 1, kBarSpFree = kBarSFull + 2, kBarOReady = kBarSpFree + 2,
               kBarXFull = kBarOReady + 2, kBarXFree = kBarXFull + 1, kBarPvDone = kBarXFree + 1,
               kBarPvFinal = kBarPvDone + 1, kBarMmaFin = kBarPvFinal + 1, kBarMmaFin2 = kBarMmaFin + 1,
-              kBarQLoad = kBarMmaFin2 + 1, kBarSRead = kBarQLoad + 1, kNumBars = kBarSRead + 2;
+              kBarQLoad = kBarMmaFin2 + 1, kNumBars = kBarQLoad + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 128 + 1024;        // + alignment slack
 static_assert(8 + 4 * kWarps <= 128, "misc area");
@@ -166,7 +172,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarQReady], 128);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kBarSFull + x], 1);     // QK^T of the tile in this score buffer done
-      mbar_init(&bars[kBarSpFree + x], 1);    // P.V reading this buffer's probabilities done
+      mbar_init(&bars[kBarSpFree + x], 8);    // the 4 sender and 4 softmax warps read this buffer
       mbar_init(&bars[kBarOReady + x], 128);  // probabilities in TMEM and O rescaled
     }
     mbar_init(&bars[kBarXFull], 1);           // arming arrival + the peer's 4 x 8 KB of partials
@@ -177,7 +183,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarMmaFin], 1);
     mbar_init(&bars[kBarMmaFin2], 1);
     mbar_init(&bars[kBarQLoad], 1);
-    for (int x = 0; x < 2; ++x) mbar_init(&bars[kBarSRead + x], 4);   // senders have read this score buffer
     *abort_s = 0;
     fence_barrier_init();
     // q of this token: latent columns [256c, 256c+256) as four SW128 boxes into the
@@ -317,25 +322,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_tiles && !*abort_s; ++i) {
       const int bb = i & 1;
       // full scores of tile i = our partials (in this tile's TMEM score buffer) + the
-      // peer's (in X); both CTAs form the same fp32 sums
-      if (!wait_warp_cluster(&bars[kBarXFull], i & 1)) { fail(); break; }
-      if (warp == 0 && lane == 0 && i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+      // peer's (in X); both CTAs form the same fp32 sums.  Our partials are read first,
+      // which frees the score buffer for QK^T of tile i+2 without waiting for the peer.
       if (!wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); break; }
       tc_fence_after();
+      uint32_t v[4][16];
+#pragma unroll
+      for (int c4 = 0; c4 < kNt / 16; ++c4) tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v[c4]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarSpFree + bb]);
+      if (!wait_warp_cluster(&bars[kBarXFull], i & 1)) { fail(); break; }
+      if (warp == 0 && lane == 0 && i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
       float s[kNt];
-      {
-        uint32_t v[4][16];
 #pragma unroll
-        for (int c4 = 0; c4 < kNt / 16; ++c4) tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v[c4]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < kNt / 4; ++k) {
-          const float4 x = *reinterpret_cast<const float4*>(xin + ((k ^ (head & 15)) * 16));
-          s[4 * k] = __uint_as_float(v[k >> 2][4 * (k & 3)]) + x.x;
-          s[4 * k + 1] = __uint_as_float(v[k >> 2][4 * (k & 3) + 1]) + x.y;
-          s[4 * k + 2] = __uint_as_float(v[k >> 2][4 * (k & 3) + 2]) + x.z;
-          s[4 * k + 3] = __uint_as_float(v[k >> 2][4 * (k & 3) + 3]) + x.w;
-        }
+      for (int k = 0; k < kNt / 4; ++k) {
+        const float4 x = *reinterpret_cast<const float4*>(xin + ((k ^ (head & 15)) * 16));
+        s[4 * k] = __uint_as_float(v[k >> 2][4 * (k & 3)]) + x.x;
+        s[4 * k + 1] = __uint_as_float(v[k >> 2][4 * (k & 3) + 1]) + x.y;
+        s[4 * k + 2] = __uint_as_float(v[k >> 2][4 * (k & 3) + 2]) + x.z;
+        s[4 * k + 3] = __uint_as_float(v[k >> 2][4 * (k & 3) + 3]) + x.w;
       }
       // our reads of the peer's partials are complete: a relaxed arrive tells the peer
       // it may overwrite X with the next tile
@@ -379,24 +386,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < w2; ++j) sm[j] += sm[j + w2];
       l_sum = l_sum * alpha + sm[0];
-      // probabilities (bf16 pairs) overwrite the first 32 columns of this tile's score
-      // buffer, once the sender warps have read our partials out of it
-      if (!wait_warp(&bars[kBarSRead + bb], (i >> 1) & 1)) { fail(); break; }
-      tc_fence_after();
-      {
-        uint32_t v[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = pk[k];
-        tmem_st16(lane_base + kColS + kNt * bb, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = pk[16 + k];
-        tmem_st16(lane_base + kColS + kNt * bb + 16, v);
-      }
-      // rescale this warp's O rows if any of its heads' reference max moved (P.V of
-      // the previous tile must be complete first)
-      if (i >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+      // P.V of the previous tile has read the P tile (and O may be rescaled)
+      if (i >= 1) {
         if (!wait_warp(&bars[kBarPvDone], (i - 1) & 1)) { fail(); break; }
         tc_fence_after();
+      }
+      // probabilities (bf16 pairs): this head's row of the K-major SW128 P tile
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(smem + kOffP + head * 128 + ((c ^ (head & 7)) * 16)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      // rescale this warp's O rows if any of its heads' reference max moved
+      if (i >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int c16 = 0; c16 < 256 / 16; ++c16) {
           uint32_t v[16];
@@ -506,8 +508,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int qd = warp & 3;
     const int head = qd * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-    char* xout = smem + kOffXStage + head * 256;
-    char* xout_warp = smem + kOffXStage + qd * kXWarpBytes;
+    char* xout = smem + kOffXStage + qd * kXHalfBytes + (lane & 15) * 256;   // this lane's staging row
+    char* xout_warp = smem + kOffXStage + qd * kXHalfBytes;
     const uint32_t xdst_warp = mapa(smem + kOffX + qd * kXWarpBytes, peer);
     const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
     // the staging rows held q until the softmax warps moved it into TMEM
@@ -522,21 +524,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarSRead + bj]);
-      if (j >= 1 && lane == 0) bulk_wait_read<0>();   // previous copy has left the staging rows
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        *reinterpret_cast<uint4*>(xout + ((k ^ (head & 15)) * 16)) =
-            make_uint4(v[k >> 2][4 * (k & 3)], v[k >> 2][4 * (k & 3) + 1], v[k >> 2][4 * (k & 3) + 2],
-                       v[k >> 2][4 * (k & 3) + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarSpFree + bj]);
       // the peer's X buffer holds its q (j = 0) or tile j-1 until all its warps have read it
       if (!(ok = wait_warp_cluster(&bars[kBarXFree], j & 1))) break;
-      if (lane == 0) {
-        bulk_copy_s2cluster(xdst_warp, xout_warp, kXWarpBytes, xfull_peer);
-        bulk_commit_group();
+      // heads 0-15 of this warp, then heads 16-31, through one 4 KB staging slot
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (lane == 0 && (j >= 1 || hh == 1)) bulk_wait_read<0>();   // the slot's last copy has read it
+        __syncwarp();
+        if ((lane >> 4) == hh) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            *reinterpret_cast<uint4*>(xout + ((k ^ (head & 15)) * 16)) =
+                make_uint4(v[k >> 2][4 * (k & 3)], v[k >> 2][4 * (k & 3) + 1], v[k >> 2][4 * (k & 3) + 2],
+                           v[k >> 2][4 * (k & 3) + 3]);
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          bulk_copy_s2cluster(xdst_warp + hh * kXHalfBytes, xout_warp, kXHalfBytes, xfull_peer);
+          bulk_commit_group();
+        }
       }
       __syncwarp();
     }
@@ -555,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
           const int s = n % kStages, bb = n & 1;
           if (!(ok = mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl))) break;
-          // the score buffer is free once P.V of tile n-2 has read its probabilities
+          // the score buffer is free once the senders and the softmax have read tile n-2
           if (n >= 2 && !(ok = mbar_wait(&bars[kBarSpFree + bb], ((n >> 1) - 1) & 1, wl))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * kStageBytes);
@@ -572,6 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
+        const uint32_t p_tile = smem_u32(smem + kOffP);
         for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
           const int s = n % kStages, bb = n & 1;
           if (!(ok = mbar_wait(&bars[kBarOReady + bb], (n >> 1) & 1, wl))) break;
@@ -579,10 +588,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t st = smem_u32(smem + s * kStageBytes);
 #pragma unroll
           for (int k = 0; k < kNt / 16; ++k)
-            mma_ts(tmem + kColO, tmem + kColS + kNt * bb + 8 * k,
+            mma_ss(tmem + kColO, smem_desc(p_tile + 32 * k, 16, 1024, kSwizzle128),
                    smem_desc(st + 2048 * k, kLatBlk, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bars[kBarKvEmpty + s]);
-          mma_commit(&bars[kBarSpFree + bb]);
           mma_commit(&bars[kBarPvDone]);
           if (n == n_tiles - 1) mma_commit(&bars[kBarPvFinal]);
         }
