@@ -170,7 +170,7 @@ sfa_status sfa_decode(const void* q, const void* kv, const int32_t* block_table,
   p.wait_limit = wl > 0 ? wl : kDefaultWaitLimit;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool tc = use_tc(h, block_size) && sfa::tc_supports_ptrs(q, kv);
+  const bool tc = use_tc(h, block_size) && sfa::tc_supports_ptrs(q, kv, p.out);
   cudaError_t e = tc ? sfa::launch_decode_tc(p, s) : sfa::launch_decode_simt(p, s);
   if (e != cudaSuccess) return SFA_ERR_CUDA;
   if (merge_after) {

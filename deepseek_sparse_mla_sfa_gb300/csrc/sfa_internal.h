@@ -63,8 +63,8 @@ cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n
 
 // tcgen05 path: whether it handles this problem, its workspace, and its launch.
 bool tc_supports(int h, int block_size);
-// the tcgen05 path also needs 16-byte aligned q and kv (TMA tensor maps)
-bool tc_supports_ptrs(const void* q, const void* kv);
+// the tcgen05 path also needs 16-byte aligned q, kv and out (TMA tensor maps)
+bool tc_supports_ptrs(const void* q, const void* kv, const void* out);
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits);
 int tc_launches(int T, int h, int top_k, int n_splits);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);

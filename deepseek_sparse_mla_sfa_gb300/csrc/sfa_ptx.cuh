@@ -155,6 +155,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
+// store a box of a 3D tensor from shared memory (bulk-group completion)
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // gather four rows (r0..r3) of a 2D tensor, columns [x, x + box_x), into four
 // consecutive box rows in shared memory, completing on `bar`
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int r0, int r1,

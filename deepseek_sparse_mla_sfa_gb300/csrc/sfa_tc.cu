@@ -71,6 +71,8 @@ constexpr int kXStageBytes = 4 * kXHalfBytes;
 constexpr int kOffP = kOffXStage + kXStageBytes;        // P [128 heads x 64 rows] bf16, K-major SW128
 constexpr int kPBytes = kHeads * kNt * 2;
 constexpr int kQBox = kHeads * 128;                     // one 64-column SW128 box of q's latent half
+constexpr int kOutBox = kHeads * 128;                   // one 32-column SW128 box of out (fp32)
+static_assert(8 * kOutBox <= kStages * kStageBytes, "out is staged in the gather stages");
 static_assert(4 * kQBox == kXBytes + kXStageBytes + kPBytes, "q's latent half fills X, staging and P");
 static_assert(kOffX % 1024 == 0 && kOffP % 1024 == 0, "SW128 operands need 1024-byte alignment");
 constexpr int kOffList = kOffP + kPBytes;
@@ -139,7 +141,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_lat,
                      const __grid_constant__ CUtensorMap tmap_rope,
                      const __grid_constant__ CUtensorMap tmap_qlat,
-                     const __grid_constant__ CUtensorMap tmap_qrope, const TcParams tp) {
+                     const __grid_constant__ CUtensorMap tmap_qrope,
+                     const __grid_constant__ CUtensorMap tmap_out, const TcParams tp) {
   const DecodeParams& p = tp.p;
   extern __shared__ char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -415,37 +418,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: out = O / l for this CTA's 256 columns; lse from CTA 0 --------
-    float* out = p.out + ((size_t)r * T + t) * p.h * kDV + 256 * crank;
-    float* lse = p.lse + ((size_t)r * T + t) * p.h;
-    if (n_tiles == 0) {
-      if (head_ok) {
-        float4* o4 = reinterpret_cast<float4*>(out + (size_t)head * kDV);
-        for (int k = 0; k < 64; ++k) o4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (crank == 0) lse[head] = -INFINITY;
-      }
-    } else if (!*abort_s) {
+    // The normalised rows are staged in the (idle) gather stages as eight SW128 boxes
+    // of 32 columns and written by TMA, one 16 KB box per store.  Every softmax warp
+    // reaches the named barrier, whatever happened before; the stores are issued only
+    // when no wait of this CTA gave up.
+    const bool aborted = *abort_s;
+    bool have_o = false;
+    if (n_tiles > 0 && !aborted) {
       // a dedicated one-phase barrier: pv_done may still be two phases behind here
-      if (!wait_warp(&bars[kBarPvFinal], 0)) {
-        fail();
-      } else {
-        tc_fence_after();
-        const float inv = 1.f / l_sum;
-        float4* o4 = reinterpret_cast<float4*>(out + (size_t)head * kDV);
+      have_o = wait_warp(&bars[kBarPvFinal], 0);
+      if (!have_o) fail();
+    }
+    if (have_o || n_tiles == 0) {
+      tc_fence_after();
+      const float inv = n_tiles > 0 ? 1.f / l_sum : 0.f;
 #pragma unroll 1
-        for (int c16 = 0; c16 < 256 / 16; ++c16) {
-          uint32_t v[16];
+      for (int c16 = 0; c16 < 256 / 16; ++c16) {
+        uint32_t v[16];
+        if (n_tiles > 0) {
           tmem_ld16(lane_base + kColO + 16 * c16, v);
           tmem_ld_wait();
-          if (head_ok) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              o4[4 * c16 + k] = make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                                            __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
-          }
         }
-        if (crank == 0 && head_ok) lse[head] = (m_ref + __log2f(l_sum)) * kLn2;
+        char* box = smem + (c16 >> 1) * kOutBox + head * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ch = 4 * (c16 & 1) + k;
+          const float4 o = n_tiles > 0 ? make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                                                     __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(box + ((ch ^ (head & 7)) * 16)) = o;
+        }
       }
+      if (crank == 0 && head_ok)
+        p.lse[((size_t)r * T + t) * p.h + head] = n_tiles > 0 ? (m_ref + __log2f(l_sum)) * kLn2 : -INFINITY;
+      fence_proxy_async_smem();
     }
+    named_barrier(2, 128);
+    if (warp == 0 && lane == 0 && !*abort_s) {
+      for (int b = 0; b < 8; ++b) tma_store_3d(&tmap_out, smem_u32(smem + b * kOutBox), 256 * crank + 32 * b, 0, r * T + t);
+      bulk_commit_group();
+      bulk_wait<0>();
+    }
+    __syncwarp();
   } else if (warp < kProducerWarp + kProducerWarps) {
     // =================== gathers ===================================================
     // Producer warp pw issues, from one lane, the gathers of row groups g = pw, pw+4,
@@ -644,6 +658,18 @@ bool make_q_map(CUtensorMap* m, const void* q, int h, long long T, int q_rows, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// out [n_tok, h, 512] fp32 as a 3D tensor; one box = 32 columns of q_rows heads of one token
+bool make_out_map(CUtensorMap* m, float* out, int h, long long n_tok, int q_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kDV, (cuuint64_t)h, (cuuint64_t)n_tok};
+  cuuint64_t strides[2] = {(cuuint64_t)kDV * 4, (cuuint64_t)h * kDV * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)q_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_row_map(CUtensorMap* m, const void* kv, int num_rows, int box_cols, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -663,9 +689,9 @@ bool tc_supports(int h, int block_size) {
   return h >= 1 && h <= kHeads;
 }
 
-bool tc_supports_ptrs(const void* q, const void* kv) {
+bool tc_supports_ptrs(const void* q, const void* kv, const void* out) {
   // tensor maps want 16-byte aligned base addresses
-  return (reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(kv) & 15) == 0;
+  return ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(kv) | reinterpret_cast<uintptr_t>(out)) & 15) == 0;
 }
 
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits) {
@@ -688,11 +714,12 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   tp.p = p;
   tp.num_rows = (int)num_rows;
   tp.q_rows = p.h < kHeads ? p.h : kHeads;
-  CUtensorMap lat, rope, qlat, qrope;
+  CUtensorMap lat, rope, qlat, qrope, omap;
   if (!make_row_map(&lat, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_row_map(&rope, p.kv, (int)num_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_q_map(&qlat, p.q, p.h, T, tp.q_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_q_map(&qrope, p.q, p.h, T, tp.q_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_q_map(&qrope, p.q, p.h, T, tp.q_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_out_map(&omap, p.out, p.h, T * p.n_splits, tp.q_rows))
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -702,7 +729,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, qlat, qrope, tp);
+  decode_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, qlat, qrope, omap, tp);
   return cudaGetLastError();
 }
 
