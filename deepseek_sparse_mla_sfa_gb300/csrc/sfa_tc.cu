@@ -205,8 +205,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 
   // ---- index resolution: count per warp chunk, then ordered compaction into smem ----
+  // A warp's chunk of the list is resolved 8 entries per lane at a time.  When the chunk
+  // fits in one such round (top_k <= 8 * kThreads), the resolved rows stay in registers
+  // for the ordered write; otherwise the write pass resolves them again.
   const int chunk = ((p.top_k + kWarps * 32 - 1) / (kWarps * 32)) * 32;
   const int c_begin = min(warp * chunk, p.top_k), c_end = min(c_begin + chunk, p.top_k);
+  const bool one_round = chunk <= 8 * 32;
+  int row_r[8];
   {
     int cnt = 0;
     for (int j0 = c_begin; j0 < c_end; j0 += 32 * 8) {
@@ -225,11 +230,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
+        row_r[k] = -1;
         if (blkv[k] == -3) continue;
         if (blkv[k] < 0 || blkv[k] >= p.num_blocks) {
           if (crank == 0) report_status(p.status, kStatusBadBlock);
         } else {
           ++cnt;
+          row_r[k] = blkv[k] * p.block_size + pos[k] % p.block_size;
         }
       }
     }
@@ -245,19 +252,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (w < warp) off += c;
     total += c;
   }
-  for (int j0 = c_begin; j0 < c_end && off < kListCap; j0 += 32) {
-    const int j = j0 + lane;
-    const int row = j < c_end ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
-    const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
-    const int o = off + __popc(mask & lanemask_lt());
-    if (row >= 0 && o < kListCap) list_s[o] = row;
-    off += __popc(mask);
+  if (one_round) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const unsigned mask = __ballot_sync(0xffffffffu, row_r[k] >= 0);
+      const int o = off + __popc(mask & lanemask_lt());
+      if (row_r[k] >= 0 && o < kListCap) list_s[o] = row_r[k];
+      off += __popc(mask);
+    }
+  } else {
+    for (int j0 = c_begin; j0 < c_end && off < kListCap; j0 += 32) {
+      const int j = j0 + lane;
+      const int row = j < c_end ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
+      const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+      const int o = off + __popc(mask & lanemask_lt());
+      if (row >= 0 && o < kListCap) list_s[o] = row;
+      off += __popc(mask);
+    }
   }
   tc_fence_before();
   cluster_sync();  // both CTAs' barriers are initialised before any remote access
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
   const int n_tiles = (total + kNt - 1) / kNt;
+  // partial scores cross between the CTAs in 16-head slots; only slots holding real
+  // heads (h of the padded 128) are sent
+  const uint32_t x_bytes = (uint32_t)((p.h + 15) / 16) * kXHalfBytes;
 
   auto fail = [&](void) {
     report_status(p.status, kStatusTimeout);
@@ -321,7 +341,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const char* xin = smem + kOffX + head * 256;   // the peer's partial scores of this head
 
     float m_ref = -INFINITY, l_sum = 0.f;  // running max (log2 units) and sum of this head
-    if (warp == 0 && lane == 0 && n_tiles > 0) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+    if (warp == 0 && lane == 0 && n_tiles > 0) mbar_arrive_expect_tx(&bars[kBarXFull], x_bytes);
     for (int i = 0; i < n_tiles && !*abort_s; ++i) {
       const int bb = i & 1;
       // full scores of tile i = our partials (in this tile's TMEM score buffer) + the
@@ -337,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarSpFree + bb]);
       if (!wait_warp_cluster(&bars[kBarXFull], i & 1)) { fail(); break; }
-      if (warp == 0 && lane == 0 && i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[kBarXFull], kXBytes);
+      if (warp == 0 && lane == 0 && i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[kBarXFull], x_bytes);
       float s[kNt];
 #pragma unroll
       for (int k = 0; k < kNt / 4; ++k) {
@@ -346,6 +366,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         s[4 * k + 1] = __uint_as_float(v[k >> 2][4 * (k & 3) + 1]) + x.y;
         s[4 * k + 2] = __uint_as_float(v[k >> 2][4 * (k & 3) + 2]) + x.z;
         s[4 * k + 3] = __uint_as_float(v[k >> 2][4 * (k & 3) + 3]) + x.w;
+      }
+      if (head >= p.h) {   // padding head: its slot may not have been sent
+#pragma unroll
+        for (int j = 0; j < kNt; ++j) s[j] = 0.f;
       }
       // our reads of the peer's partials are complete: a relaxed arrive tells the peer
       // it may overwrite X with the next tile
@@ -526,6 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     char* xout_warp = smem + kOffXStage + qd * kXHalfBytes;
     const uint32_t xdst_warp = mapa(smem + kOffX + qd * kXWarpBytes, peer);
     const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
+    const int n_half = min(2, max(0, (p.h - 32 * qd + 15) / 16));   // this warp's 16-head slots with real heads
     // the staging rows held q until the softmax warps moved it into TMEM
     bool ok = n_tiles == 0 || wait_warp(&bars[kBarQReady], 0);
     for (int j = 0; ok && j < n_tiles && !*abort_s; ++j) {
@@ -539,11 +564,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarSpFree + bj]);
+      if (n_half == 0) continue;   // only padding heads in this quadrant
       // the peer's X buffer holds its q (j = 0) or tile j-1 until all its warps have read it
       if (!(ok = wait_warp_cluster(&bars[kBarXFree], j & 1))) break;
       // heads 0-15 of this warp, then heads 16-31, through one 4 KB staging slot
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
+        if (hh >= n_half) break;
         if (lane == 0 && (j >= 1 || hh == 1)) bulk_wait_read<0>();   // the slot's last copy has read it
         __syncwarp();
         if ((lane >> 4) == hh) {

@@ -34,6 +34,8 @@ SMALL = [
     W("h33_bs1", B=1, Q=1, h=33, S=300, top_k=150, n_splits=1, index_kind="uniform", block_size=1, seed=14),
     W("h100_q3", B=2, Q=3, h=100, S=900, S_min=1, top_k=257, n_splits=2, index_kind="causal", seed=15),
     W("h65_spare", B=2, Q=1, h=65, S=640, top_k=640, n_splits=1, index_kind="uniform", spare_blocks=5, seed=16),
+    # more valid entries than the tcgen05 kernel keeps resolved at once (2048): list refills
+    W("h128_k3000", B=1, Q=1, h=128, S=4096, top_k=3000, n_splits=1, index_kind="uniform", seed=17),
 ]
 
 
