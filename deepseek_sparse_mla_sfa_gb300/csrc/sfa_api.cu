@@ -26,6 +26,35 @@ std::atomic<int> g_kernel_path{0};  // 0 automatic, 1 CUDA-core only
 bool use_tc(int h, int block_size) { return g_kernel_path.load() == 0 && sfa::tc_supports(h, block_size); }
 constexpr long long kDefaultWaitLimit = 1LL << 26;  // iterations of a bounded device wait
 
+// helper streams of sfa_decode_host, created once per device on first use
+constexpr int kHostGroups = 4;
+constexpr double kHostPipeMinOutBytes = 4.0 * (1 << 20);   // smaller results: one group
+struct HostPipe {
+  std::mutex mu;   // one enqueue sequence at a time uses the shared events
+  cudaStream_t s[kHostGroups] = {};
+  cudaEvent_t start = nullptr, done[kHostGroups] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe* g_pipe[kMaxDevices] = {};
+bool g_pipe_failed[kMaxDevices] = {};
+
+HostPipe* host_pipe(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  if (g_pipe[dev] || g_pipe_failed[dev]) return g_pipe[dev];
+  HostPipe* hp = new HostPipe;
+  bool ok = cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) == cudaSuccess;
+  for (int g = 0; ok && g < kHostGroups; ++g)
+    ok = cudaStreamCreateWithFlags(&hp->s[g], cudaStreamNonBlocking) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp->done[g], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    g_pipe_failed[dev] = true;   // fall back to a single group on the caller's stream
+    return nullptr;
+  }
+  g_pipe[dev] = hp;
+  return hp;
+}
+
 int* status_word(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -241,19 +270,55 @@ sfa_status sfa_decode_host(const void* q_host, const void* kv, const int32_t* bl
   void* ws_d = ws_bytes ? carve(ws_bytes) : nullptr;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(q_d, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(bt_d, block_table_host, bt_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+  // A batch large enough to be copy-bound is split into groups of whole sequences, each
+  // on its own helper stream forked from `s`: group g's results travel back while later
+  // groups are still being copied in or computed, and copies in both directions use
+  // separate copy engines.  Each group uses its own slices of the staging buffers.
+  int groups = 1;
+  HostPipe* hp = nullptr;
+  if ((double)out_bytes >= kHostPipeMinOutBytes && B >= 2) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) hp = host_pipe(dev);
+    if (hp) groups = B < kHostGroups ? B : kHostGroups;
+  }
+  // the block table, sequence lengths and index lists go first, whole, on `s`; each
+  // group then copies only its q in and its out back, and lse returns in one copy at the end
+  if (cudaMemcpyAsync(bt_d, block_table_host, bt_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(sl_d, seq_lens_host, sl_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      (idx_bytes && cudaMemcpyAsync(idx_d, topk_idx_host, idx_bytes, cudaMemcpyHostToDevice, s) !=
-                        cudaSuccess))
+      (idx_bytes && cudaMemcpyAsync(idx_d, topk_idx_host, idx_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess))
     return SFA_ERR_CUDA;
-  st = sfa_decode(q_d, kv, bt_d, sl_d, idx_d, B, Q, h, top_k, num_blocks, block_size,
-                  max_blocks_per_seq, scale, n_splits, out_d, lse_d, op_d, lp_d, ws_d, ws_bytes,
-                  stream);
-  if (st != SFA_OK) return st;
-  if (cudaMemcpyAsync(out_host, out_d, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(lse_host, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return SFA_ERR_CUDA;
+  std::unique_lock<std::mutex> lk;
+  if (groups > 1) {
+    lk = std::unique_lock<std::mutex>(hp->mu);
+    if (cudaEventRecord(hp->start, s) != cudaSuccess) return SFA_ERR_CUDA;
+  }
+  for (int g = 0; g < groups; ++g) {
+    const int b0 = (int)((long long)B * g / groups), b1 = (int)((long long)B * (g + 1) / groups);
+    const int Bg = b1 - b0;
+    if (Bg == 0) continue;
+    cudaStream_t gs = groups > 1 ? hp->s[g] : s;
+    if (groups > 1 && cudaStreamWaitEvent(gs, hp->start, 0) != cudaSuccess) return SFA_ERR_CUDA;
+    const size_t t0 = (size_t)b0 * Q, Tg = (size_t)Bg * Q;
+    const size_t qo = t0 * h * SFA_D_QK * 2, io = t0 * top_k, oo = t0 * h * SFA_D_V, lo = t0 * h;
+    const size_t bo = (size_t)b0 * max_blocks_per_seq;
+    char* qg = static_cast<char*>(q_d) + qo;
+    if (cudaMemcpyAsync(qg, static_cast<const char*>(q_host) + qo, Tg * h * SFA_D_QK * 2,
+                        cudaMemcpyHostToDevice, gs) != cudaSuccess)
+      return SFA_ERR_CUDA;
+    // a group's shard partials are its own [n_splits, Tg, h, ...] block
+    float* opg = op_d ? op_d + (size_t)n_splits * oo : nullptr;
+    float* lpg = lp_d ? lp_d + (size_t)n_splits * lo : nullptr;
+    st = sfa_decode(qg, kv, bt_d + bo, sl_d + b0, idx_d + io, Bg, Q, h, top_k, num_blocks, block_size,
+                    max_blocks_per_seq, scale, n_splits, out_d + oo, lse_d + lo, opg, lpg, ws_d, ws_bytes, gs);
+    if (st != SFA_OK) return st;
+    if (cudaMemcpyAsync(out_host + oo, out_d + oo, Tg * h * SFA_D_V * 4, cudaMemcpyDeviceToHost, gs) !=
+        cudaSuccess)
+      return SFA_ERR_CUDA;
+    if (groups > 1 && (cudaEventRecord(hp->done[g], gs) != cudaSuccess ||
+                       cudaStreamWaitEvent(s, hp->done[g], 0) != cudaSuccess))
+      return SFA_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(lse_host, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SFA_ERR_CUDA;
   return SFA_OK;
 }
 

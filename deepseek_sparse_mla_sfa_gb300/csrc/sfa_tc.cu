@@ -32,6 +32,8 @@
 // lane quadrant w % 4).  Every wait is bounded; a wait that gives up records
 // SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
 #include <cuda.h>
+#include <string.h>
+
 #include <mutex>
 
 #include "sfa_internal.h"
@@ -671,42 +673,75 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Encoded tensor maps, remembered per host thread: a serving loop passes the same cache,
+// staging and output buffers every step, so encoding happens once per buffer layout.
+struct MapKey {
+  uint64_t f[14];
+  bool operator==(const MapKey& o) const { return memcmp(f, o.f, sizeof f) == 0; }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kMapCache = 32;
+thread_local MapEntry t_maps[kMapCache];
+thread_local int t_maps_next = 0;
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
+  MapKey k;
+  memset(&k, 0, sizeof k);
+  k.f[0] = (uint64_t)dt | ((uint64_t)rank << 8) | ((uint64_t)sw << 16) | ((uint64_t)l2 << 24);
+  k.f[1] = reinterpret_cast<uint64_t>(base);
+  for (int i = 0; i < rank; ++i) {
+    k.f[2 + i] = dims[i];
+    k.f[5 + i] = box[i];
+    if (i + 1 < rank) k.f[8 + i] = strides[i];
+  }
+  for (int e = 0; e < kMapCache; ++e)
+    if (t_maps[e].used && t_maps[e].key == k) {
+      *m = t_maps[e].map;
+      return true;
+    }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  if (fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+         l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  MapEntry& slot = t_maps[t_maps_next];
+  t_maps_next = (t_maps_next + 1) % kMapCache;
+  slot.key = k;
+  slot.map = *m;
+  slot.used = true;
+  return true;
+}
+
 // q [T, h, 576] as a 3D tensor (columns, heads, tokens); one box = box_cols columns of
 // q_rows heads of one token
 bool make_q_map(CUtensorMap* m, const void* q, int h, long long T, int q_rows, int box_cols, CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)h, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)h * kDQK * 2};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)q_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 // out [n_tok, h, 512] fp32 as a 3D tensor; one box = 32 columns of q_rows heads of one token
 bool make_out_map(CUtensorMap* m, float* out, int h, long long n_tok, int q_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kDV, (cuuint64_t)h, (cuuint64_t)n_tok};
   cuuint64_t strides[2] = {(cuuint64_t)kDV * 4, (cuuint64_t)h * kDV * 4};
   cuuint32_t box[3] = {32, (cuuint32_t)q_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
+// the cache as [num_rows, 576] rows; one box = box_cols columns of one row (gathered four at a time)
 bool make_row_map(CUtensorMap* m, const void* kv, int num_rows, int box_cols, CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)num_rows};
   cuuint64_t strides[1] = {(cuuint64_t)kDQK * 2};
   cuuint32_t box[2] = {(cuuint32_t)box_cols, 1};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 }  // namespace

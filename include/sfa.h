@@ -141,6 +141,14 @@ sfa_status sfa_lse_merge(const float *out_part, const float *lse_part, int n_spl
  *   staging      device scratch of at least sfa_decode_host_staging_bytes(...) bytes,
  *                256-byte aligned; holds the device copies, partials and workspace.
  * Host buffers must stay valid until the stream reaches the end of the copies.
+ *
+ * A batch whose out is at least 4 MiB is processed as up to 4 groups of whole
+ * sequences.  Each group runs on a helper stream that the library creates once per
+ * device, forked from `stream` by an event and joined back into it, so the call stays
+ * ordered on `stream`.  A group's result copies overlap later groups' input copies
+ * and kernels.  Calls from several host threads take turns at enqueueing (a mutex),
+ * and their groups share the helper streams.  If an error is returned after some
+ * groups were enqueued, that work may still run.
  */
 size_t sfa_decode_host_staging_bytes(int B, int Q, int h, int top_k, int max_blocks_per_seq,
                                      int n_splits);

@@ -235,6 +235,31 @@ def test_host_buffer_entry_point_matches_device_entry_point():
     assert torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())
 
 
+@pytest.mark.parametrize("n_splits", [1, 3])
+def test_host_buffer_entry_point_in_sequence_groups(n_splits):
+    # out >= 4 MiB: the host entry point splits the batch into groups of sequences on
+    # helper streams; the result must be the device entry point's, bit for bit
+    w = W("host_groups", B=13, Q=2, h=128, S=4000, S_min=300, top_k=400, n_splits=n_splits,
+          index_kind="causal", seed=29 + n_splits)
+    inp = workloads.make(w, device="cuda")
+    out, lse = run_cuda(inp)
+    pin = lambda t: t.cpu().pin_memory()
+    out_h = torch.full((w.T, w.h, 512), float("nan"), dtype=torch.float32).pin_memory()
+    lse_h = torch.full((w.T, w.h), float("nan"), dtype=torch.float32).pin_memory()
+    nbytes = sfa.decode_host_staging_bytes(w.B, w.Q, w.h, w.top_k, inp.max_blocks, w.n_splits)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()   # the inputs exist before the side stream reads them
+    for stream in (None, side):
+        sfa.decode_host(pin(inp.q), inp.kv, pin(inp.block_table), pin(inp.seq_lens), pin(inp.topk_idx),
+                        w.scale, w.n_splits, w.Q, out_h, lse_h, staging, stream=stream)
+        (side if stream is not None else torch.cuda.current_stream()).synchronize()
+        assert torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())
+        out_h.fill_(float("nan"))
+        lse_h.fill_(float("nan"))
+    assert sfa.last_device_status() == 0
+
+
 def test_tensor_core_kernel_serves_every_workload():
     for name, w in workloads.CONFIGS.items():
         n, tc = sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits, merge=False)
