@@ -214,6 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int c_begin = min(warp * chunk, p.top_k), c_end = min(c_begin + chunk, p.top_k);
   const bool one_round = chunk <= 8 * 32;
   int row_r[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) row_r[k] = -1;   // warps with an empty chunk write nothing
   {
     int cnt = 0;
     for (int j0 = c_begin; j0 < c_end; j0 += 32 * 8) {
@@ -459,20 +461,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = n_tiles > 0 ? 1.f / l_sum : 0.f;
 #pragma unroll 1
-      for (int c16 = 0; c16 < 256 / 16; ++c16) {
-        uint32_t v[16];
+      for (int c64 = 0; c64 < 256 / 64; ++c64) {   // 64 columns per round: four TMEM loads in flight
+        uint32_t v[4][16];
         if (n_tiles > 0) {
-          tmem_ld16(lane_base + kColO + 16 * c16, v);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tmem_ld16(lane_base + kColO + 64 * c64 + 16 * u, v[u]);
           tmem_ld_wait();
         }
-        char* box = smem + (c16 >> 1) * kOutBox + head * 128;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int ch = 4 * (c16 & 1) + k;
-          const float4 o = n_tiles > 0 ? make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                                                     __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4*>(box + ((ch ^ (head & 7)) * 16)) = o;
+        for (int u = 0; u < 4; ++u) {
+          const int c16 = 4 * c64 + u;
+          char* box = smem + (c16 >> 1) * kOutBox + head * 128;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int ch = 4 * (c16 & 1) + k;
+            const float4 o = n_tiles > 0 ? make_float4(__uint_as_float(v[u][4 * k]) * inv, __uint_as_float(v[u][4 * k + 1]) * inv,
+                                                       __uint_as_float(v[u][4 * k + 2]) * inv, __uint_as_float(v[u][4 * k + 3]) * inv)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(box + ((ch ^ (head & 7)) * 16)) = o;
+          }
         }
       }
       if (crank == 0 && head_ok)
@@ -483,7 +490,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0 && !*abort_s) {
       for (int b = 0; b < 8; ++b) tma_store_3d(&tmap_out, smem_u32(smem + b * kOutBox), 256 * crank + 32 * b, 0, r * T + t);
       bulk_commit_group();
-      bulk_wait<0>();
+      bulk_wait_read<0>();   // shared memory may be released once read; the writes finish with the grid
     }
     __syncwarp();
   } else if (warp < kProducerWarp + kProducerWarps) {
