@@ -200,6 +200,29 @@ def decode_host(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, scal
     return out_host, lse_host
 
 
+def kv_write(kv, slot_mapping, rows, stream=None):
+    """Latent-cache write (C ABI ``sfa_kv_write``): kv viewed as [num_blocks*block_size, 576]
+    gets row slot_mapping[t] = rows[t] for every t with slot_mapping[t] >= 0, in place.
+
+    kv [num_blocks, block_size, 576] bf16, slot_mapping [T] int32, rows [T, 576] bf16, all on
+    one CUDA device.  Returns kv.
+    """
+    lib = _lib.load()
+    dev = kv.device
+    if dev.type != "cuda":
+        raise ValueError("kv_write runs on a CUDA device only")
+    _need(kv, "kv", torch.bfloat16, dev, 3)
+    _need(slot_mapping, "slot_mapping", torch.int32, dev, 1)
+    _need(rows, "rows", torch.bfloat16, dev, 2)
+    if kv.shape[2] != D_QK or rows.shape[1] != D_QK or rows.shape[0] != slot_mapping.shape[0]:
+        raise ValueError("rows must be [T, 576] with one slot per row")
+    num_slots = kv.shape[0] * kv.shape[1]
+    code = lib.sfa_kv_write(_ptr(kv), num_slots, _ptr(slot_mapping), _ptr(rows), rows.shape[0],
+                            _stream_ptr(stream, dev))
+    _lib.check("sfa_kv_write", code)
+    return kv
+
+
 def decode_launches(B, Q, h, top_k, block_size, n_splits, merge=True):
     """(kernels one decode call enqueues, whether the tcgen05 kernel serves it)."""
     tc = ctypes.c_int(0)

@@ -322,6 +322,22 @@ sfa_status sfa_decode_host(const void* q_host, const void* kv, const int32_t* bl
   return SFA_OK;
 }
 
+sfa_status sfa_kv_write(void* kv, long long num_slots, const int32_t* slot_mapping, const void* rows, int T,
+                        sfa_stream stream) {
+  if (T < 0 || num_slots < 0) return SFA_ERR_INVALID_ARG;
+  if (T == 0) return SFA_OK;
+  if (!kv || !slot_mapping || !rows || !aligned(kv, 16) || !aligned(rows, 16) || !aligned(slot_mapping, 4))
+    return SFA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
+  int* status = status_word(dev);
+  if (!status) return SFA_ERR_CUDA;
+  return sfa::launch_kv_write(kv, num_slots, slot_mapping, rows, T, status, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
+}
+
 sfa_status sfa_last_device_status(sfa_stream stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;

@@ -128,6 +128,25 @@ sfa_status sfa_lse_merge(const float *out_part, const float *lse_part, int n_spl
                          int dv, float *out, float *lse, sfa_stream stream);
 
 /*
+ * sfa_kv_write -- the latent-cache write that precedes attention: each new token's
+ * latent row (kv_lora_rank + qk_rope_head_dim = 576 bf16) is stored at the cache slot
+ * slot_mapping[t] ("RFC: MsModeling 支持 Decode Context Parallel 仿真", 2.1.4.1:
+ * slot_mapping [total_num_tokens] int32; 1.3: the fused pre-attention op writes the
+ * KV).  A slot is block * block_size + offset, i.e. a row of the cache seen as
+ * [num_blocks * block_size, 576].
+ *
+ *   kv            device bf16 [num_blocks, block_size, 576] (num_slots rows), written in place
+ *   slot_mapping  device int32 [T]: the slot of each new token; < 0 = padding (skipped)
+ *   rows          device bf16 [T, 576]: the new latent rows
+ *   T >= 0, num_slots >= 0; kv and rows 16-byte aligned.
+ * Two tokens naming the same slot leave one of their rows there (which one is not
+ * defined).  A slot >= num_slots writes nothing and sets SFA_ERR_DEVICE_BAD_BLOCK in
+ * the device status word.  Returns SFA_OK or a host-side argument error, nothing launched.
+ */
+sfa_status sfa_kv_write(void *kv, long long num_slots, const int32_t *slot_mapping, const void *rows, int T,
+                        sfa_stream stream);
+
+/*
  * sfa_decode_host -- one decode step whose per-step inputs and outputs live in
  * host memory, with the latent cache resident on the device (the form a serving
  * loop that keeps its cache in HBM uses).  Enqueues on `stream`: host->device

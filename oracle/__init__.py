@@ -58,6 +58,8 @@ def _bind(path: str):
     lib.sfa_oracle_decode_sampled.restype = I
     lib.sfa_oracle_merge.argtypes = [P, P, I, ctypes.c_long, I, P, P]
     lib.sfa_oracle_merge.restype = I
+    lib.sfa_oracle_kv_write.argtypes = [P, ctypes.c_long, P, P, ctypes.c_long, I]
+    lib.sfa_oracle_kv_write.restype = I
     return lib
 
 
@@ -181,3 +183,21 @@ def merge(out_part, lse_part):
     if rc != 0:
         raise RuntimeError(f"sfa_oracle_merge failed ({rc})")
     return out, lse
+
+
+def kv_write(kv, slot_mapping, rows):
+    """The latent-cache write (slot_mapping scatter): returns a copy of `kv` (bf16 bits or
+    tensor [num_blocks, block_size, 576]) with row slot_mapping[t] replaced by rows[t]
+    for every t whose slot is >= 0.  Raises on a slot past the cache or a repeated slot."""
+    lib = _load()
+    kvb = _as_bf16_bits(kv).copy()
+    sm = _as_i32(slot_mapping)
+    rb = _as_bf16_bits(rows)
+    D = kvb.shape[-1]
+    num_slots = kvb.size // D
+    if rb.ndim != 2 or (rb.shape[0] and rb.shape[1] != D) or sm.shape[0] != rb.shape[0]:
+        raise ValueError("rows must be [T, D] with one slot per row")
+    rc = lib.sfa_oracle_kv_write(_ptr(kvb), num_slots, _ptr(sm), _ptr(rb), int(sm.shape[0]), int(D))
+    if rc != 0:
+        raise ValueError("slot past the cache or repeated slot")
+    return kvb

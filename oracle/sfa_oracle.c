@@ -378,3 +378,36 @@ int sfa_oracle_merge(const double *out_part, const double *lse_part, int n, long
   }
   return ORACLE_OK;
 }
+
+/*
+ * Latent-cache write: the slot_mapping scatter by which the fused pre-attention op
+ * stores each new token's latent row ("RFC: MsModeling 支持 Decode Context Parallel
+ * 仿真", 2.1.4.1: slot_mapping is [total_num_tokens] int32, one physical cache slot
+ * per new token; 1.3: the fused RMSNorm + QKV proj + RoPE + KV-write op writes the
+ * local cache).
+ *
+ *   for each new token t:  slot = slot_mapping[t]
+ *     slot < 0            ->  padding, nothing is written
+ *     0 <= slot < slots   ->  kv[slot, 0:D] = rows[t, 0:D]   (bit copy)
+ *
+ * kv is the cache seen as [num_slots, D] rows (num_slots = N_blk * block_size).
+ * Returns ORACLE_ERR_ARG, writing nothing, when a slot is >= num_slots or when two
+ * tokens name the same slot (the write order would then decide the result).
+ */
+int sfa_oracle_kv_write(uint16_t *kv, long num_slots, const int32_t *slot_mapping, const uint16_t *rows,
+                        long T, int D) {
+  if (!kv || !slot_mapping || (!rows && T > 0) || num_slots < 0 || T < 0 || D < 1) return ORACLE_ERR_ARG;
+  for (long t = 0; t < T; ++t) {
+    const long s = slot_mapping[t];
+    if (s >= num_slots) return ORACLE_ERR_ARG;
+    if (s < 0) continue;
+    for (long u = 0; u < t; ++u)
+      if (slot_mapping[u] == slot_mapping[t]) return ORACLE_ERR_ARG;
+  }
+  for (long t = 0; t < T; ++t) {
+    const long s = slot_mapping[t];
+    if (s < 0) continue;
+    for (int d = 0; d < D; ++d) kv[(size_t)s * D + d] = rows[(size_t)t * D + d];
+  }
+  return ORACLE_OK;
+}

@@ -43,6 +43,14 @@ MUTANTS = [
     ("no_dedup_semantics", "long pos = idx[j];\n    if (pos < lo || pos >= hi) continue;",
      "long pos = idx[j];\n    if (pos < lo || pos >= hi) continue;\n    if (j > 0 && idx[j - 1] == pos) continue;",
      [pins.test_duplicate_entries_count_once_per_list_entry]),
+    ("kv_write_next_slot", "for (int d = 0; d < D; ++d) kv[(size_t)s * D + d] = rows[(size_t)t * D + d];",
+     "for (int d = 0; d < D; ++d) kv[(size_t)(s + 1 < num_slots ? s + 1 : s) * D + d] = rows[(size_t)t * D + d];",
+     [pins.test_kv_write_places_rows_skips_padding_and_leaves_the_rest,
+      pins.test_decode_after_write_reads_the_new_token_row]),
+    ("kv_write_writes_padding",
+     "    const long s = slot_mapping[t];\n    if (s < 0) continue;\n    for (int d = 0; d < D; ++d)",
+     "    const long s = slot_mapping[t] < 0 ? 0 : slot_mapping[t];\n    for (int d = 0; d < D; ++d)",
+     [pins.test_kv_write_places_rows_skips_padding_and_leaves_the_rest]),
     ("padding_minus_one_only", "if (pos < lo || pos >= hi) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
      "if (pos == -1) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
      [pins.test_empty_selection_gives_zero_and_minus_inf]),

@@ -352,3 +352,65 @@ def test_sampled_pairs_match_full_decode():
     so, sl = oracle.decode_sampled(prob, t, hh, shards=r, n_splits=3)
     np.testing.assert_array_equal(so, op[r, t, hh])
     np.testing.assert_array_equal(sl, lp[r, t, hh])
+
+
+# --------------------------------------------------------------------------------------
+# latent-cache write (slot_mapping scatter)
+# --------------------------------------------------------------------------------------
+def _cache_and_rows(seed, num_blocks=6, bs=16, T=20):
+    rng = np.random.default_rng(seed)
+    kv = rng.integers(0, 1 << 16, size=(num_blocks, bs, D_QK), dtype=np.uint16)
+    rows = rng.integers(0, 1 << 16, size=(T, D_QK), dtype=np.uint16)
+    slots = rng.permutation(num_blocks * bs)[:T].astype(np.int32)
+    slots[::5] = -1                                   # padding entries
+    return kv, rows, slots
+
+
+def test_kv_write_places_rows_skips_padding_and_leaves_the_rest():
+    kv, rows, slots = _cache_and_rows(40)
+    out = oracle.kv_write(kv, slots, rows).reshape(-1, D_QK)
+    flat = kv.reshape(-1, D_QK)
+    written = {int(s): t for t, s in enumerate(slots) if s >= 0}
+    for s in range(flat.shape[0]):
+        expect = rows[written[s]] if s in written else flat[s]
+        assert np.array_equal(out[s], expect)
+
+
+def test_kv_write_is_order_independent_and_idempotent():
+    kv, rows, slots = _cache_and_rows(41)
+    once = oracle.kv_write(kv, slots, rows)
+    perm = np.random.default_rng(3).permutation(len(slots))
+    assert np.array_equal(oracle.kv_write(kv, slots[perm], rows[perm]), once)
+    assert np.array_equal(oracle.kv_write(once, slots, rows), once)
+
+
+def test_kv_write_rejects_slots_past_the_cache_and_repeated_slots():
+    kv, rows, slots = _cache_and_rows(42)
+    bad = slots.copy()
+    bad[3] = kv.shape[0] * kv.shape[1]
+    with pytest.raises(ValueError):
+        oracle.kv_write(kv, bad, rows)
+    rep = slots.copy()
+    rep[4] = rep[1] if rep[1] >= 0 else 0
+    rep[1] = rep[4]
+    with pytest.raises(ValueError):
+        oracle.kv_write(kv, rep, rows)
+
+
+def test_decode_after_write_reads_the_new_token_row():
+    # sequence 1 gets a new token at position L (its cache grows to L + 1); its slot is
+    # block_table[1, L // bs] * bs + L % bs.  Attending only to it with q = 0 returns
+    # exactly the new row's latent part and lse = ln 1 = 0.
+    bs, L = 16, 37
+    dense = rng_normal((2, 64, D_QK), 43)
+    prob, pg = problem(dense, [50, L + 1], np.zeros((2, 3, D_QK), np.float32), [[0], [0]], bs=bs,
+                       perm_seed=7)
+    new_row = rng_normal((1, D_QK), 44)
+    slot = int(pg.block_table[1, L // bs]) * bs + L % bs
+    kv2 = oracle.kv_write(pg.kv, np.array([slot], np.int32), bf16_bits(new_row))
+    prob2 = oracle.Problem(bf16_bits(np.zeros((2, 3, D_QK), np.float32)), kv2, pg.block_table, pg.seq_lens,
+                           np.array([[0], [L]], np.int32), 1, SCALE)
+    out, lse = oracle.decode(prob2)
+    for hh in range(3):
+        assert np.array_equal(out[1, hh], bf(new_row[0, :D_V]))
+        assert lse[1, hh] == 0.0
