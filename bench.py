@@ -317,6 +317,7 @@ def run_ours(args, world, rank, local):
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         cpu, _ = cpu_oracle_leg(inp, acc, target_s=15.0)
+    next_rows = None if args.no_next_rows else measure_next_rows(sfa, inp, peaks, flush)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -337,10 +338,62 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": launches_per_step * args.steps,
+        "next_rows": next_rows,
         "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def measure_next_rows(sfa, inp, peaks, flush):
+    """The rows after the decode step at this workload's shapes, each timed alone with CUDA
+    events on the launching stream (L2 scrubbed before each launch):
+      kv_write - the T new tokens' latent rows scattered into the cache at their slots;
+      uv_proj  - the W_UV up-projection of the decode output (synthetic weights)."""
+    w = inp.w
+    dev = inp.q.device
+    T, h = w.T, w.h
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 99)
+    num_slots = inp.kv.shape[0] * inp.kv.shape[1]
+    slots = torch.randperm(num_slots, generator=g)[:T].to(torch.int32).to(dev)
+    rows = torch.randn((T, 576), generator=g).to(torch.bfloat16).to(dev)
+    kv_copy = inp.kv  # written in place: the rows land in slots no decode of this run reads again
+    out = torch.randn((T, h, 512), generator=g).to(dev) * 0.3
+    w_uv = (torch.randn((h, 512, 128), generator=g) / 512 ** 0.5).to(torch.bfloat16).to(dev)
+    y = torch.empty((T, h, 128), dtype=torch.bfloat16, device=dev)
+
+    def timed(fn, n):
+        # the L2 scrub before each call also keeps the stream busy while the host enqueues
+        # the call, so the events bracket device time only
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / n * 1e-3   # seconds
+
+    t_kv = timed(lambda: sfa.kv_write(kv_copy, slots, rows), 30)
+    t_uv = timed(lambda: sfa.uv_proj(out, w_uv, y), 30)
+    if sfa.last_device_status() != 0:
+        raise RuntimeError("device status error in the next-row kernels")
+    kv_bytes = T * 1152 * 2 + T * 4
+    uv_bytes = T * h * 512 * 4 + h * 512 * 128 * 2 + T * h * 128 * 2
+    uv_flops = 2 * T * h * 512 * 128
+    uv_gbs = uv_bytes / t_uv / 1e9
+    return {
+        "kv_write": {"us": t_kv * 1e6, "rows": T, "bytes": kv_bytes, "GB/s": kv_bytes / t_kv / 1e9,
+                     "note": "latency-bound at this size (one 1152-byte row per warp)"},
+        "uv_proj": {"us": t_uv * 1e6, "shape": f"[{T},{h},512] x [{h},512,128]", "TFLOP/s": uv_flops / t_uv / 1e12,
+                    "roofline": {"bound": "hbm", "achieved": uv_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": uv_gbs / peaks["hbm_gbs"], "bytes": uv_bytes}},
+    }
 
 
 def read_traffic(kernel: str, tc_path: bool, workload: str):
@@ -401,6 +454,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip timing the kv_write / uv_proj rows after the decode step")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's B (smaller cases for profiler captures)")
     args = ap.parse_args()

@@ -200,6 +200,29 @@ def decode_host(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, scal
     return out_host, lse_host
 
 
+def uv_proj(out, w_uv, y=None, stream=None):
+    """W_UV up-projection (C ABI ``sfa_uv_proj``): y[t, h, v] = sum_c out[t, h, c] * w_uv[h, c, v].
+
+    out [T, h, 512] fp32 (decode's output), w_uv [h, 512, 128] bf16, y [T, h, 128] bf16
+    (allocated when None), all on one CUDA device.  Returns y.
+    """
+    lib = _lib.load()
+    dev = out.device
+    if dev.type != "cuda":
+        raise ValueError("uv_proj runs on a CUDA device only")
+    _need(out, "out", torch.float32, dev, 3)
+    _need(w_uv, "w_uv", torch.bfloat16, dev, 3)
+    T, h, c = out.shape
+    if c != D_V or tuple(w_uv.shape) != (h, D_V, 128):
+        raise ValueError("out must be [T, h, 512] and w_uv [h, 512, 128]")
+    if y is None:
+        y = torch.empty((T, h, 128), dtype=torch.bfloat16, device=dev)
+    _need(y, "y", torch.bfloat16, dev, 3)
+    code = lib.sfa_uv_proj(_ptr(out), _ptr(w_uv), _ptr(y), T, h, _stream_ptr(stream, dev))
+    _lib.check("sfa_uv_proj", code)
+    return y
+
+
 def kv_write(kv, slot_mapping, rows, stream=None):
     """Latent-cache write (C ABI ``sfa_kv_write``): kv viewed as [num_blocks*block_size, 576]
     gets row slot_mapping[t] = rows[t] for every t with slot_mapping[t] >= 0, in place.

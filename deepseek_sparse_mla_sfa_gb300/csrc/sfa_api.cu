@@ -322,6 +322,21 @@ sfa_status sfa_decode_host(const void* q_host, const void* kv, const int32_t* bl
   return SFA_OK;
 }
 
+sfa_status sfa_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, sfa_stream stream) {
+  if (T < 0 || h < 1 || h > 65535) return SFA_ERR_INVALID_ARG;
+  if (T == 0) return SFA_OK;
+  if (!out || !w_uv || !y || !aligned(out, 16) || !aligned(w_uv, 16) || !aligned(y, 2)) return SFA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
+  int* status = status_word(dev);
+  if (!status) return SFA_ERR_CUDA;
+  const long long wl = g_wait_limit.load();
+  return sfa::launch_uv_proj(out, w_uv, y, T, h, wl > 0 ? wl : kDefaultWaitLimit, status,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
+}
+
 sfa_status sfa_kv_write(void* kv, long long num_slots, const int32_t* slot_mapping, const void* rows, int T,
                         sfa_stream stream) {
   if (T < 0 || num_slots < 0) return SFA_ERR_INVALID_ARG;

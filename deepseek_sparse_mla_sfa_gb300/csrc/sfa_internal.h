@@ -58,6 +58,8 @@ __host__ __device__ __forceinline__ void shard_bounds(int seq_len, int L, int r,
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, long long wait_limit,
+                           int* status, cudaStream_t stream);
 cudaError_t launch_kv_write(void* kv, long long num_slots, const int32_t* slot_mapping, const void* rows, int T,
                             int* status, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,

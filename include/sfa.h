@@ -147,6 +147,23 @@ sfa_status sfa_kv_write(void *kv, long long num_slots, const int32_t *slot_mappi
                         sfa_stream stream);
 
 /*
+ * sfa_uv_proj -- the W_UV up-projection that follows attention in the latent space:
+ *   y[t, h, v] = sum_{c < 512} out[t, h, c] * w_uv[h, c, v],   v < 128
+ * (MLA attends over the 512-wide latent; W_UV, derived from kv_b_proj, takes each head's
+ * output to its 128-wide value space: "RFC: Context Parallel Modeling for
+ * DeepSeek-Style Attention", 3.5).  A tcgen05 contraction per (head, 64 tokens).
+ *
+ *   out   device fp32 [T, h, 512] (sfa_decode's out); rounded to bf16 for the tensor cores
+ *   w_uv  device bf16 [h, 512, 128]
+ *   y     device bf16 [T, h, 128]
+ *   T >= 0, 1 <= h <= 65535; out and w_uv 16-byte aligned, y 2-byte aligned.
+ * Accuracy: |y - exact| <= 2^-8 * sum_c |out[c] * w[c, v]| + 2^-8 * |exact| (bf16 inputs,
+ * fp32 accumulation, bf16 result).  A bounded wait that gives up sets
+ * SFA_ERR_DEVICE_TIMEOUT in the device status word.  Returns SFA_OK or a host-side error.
+ */
+sfa_status sfa_uv_proj(const float *out, const void *w_uv, void *y, int T, int h, sfa_stream stream);
+
+/*
  * sfa_decode_host -- one decode step whose per-step inputs and outputs live in
  * host memory, with the latent cache resident on the device (the form a serving
  * loop that keeps its cache in HBM uses).  Enqueues on `stream`: host->device

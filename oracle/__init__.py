@@ -201,3 +201,18 @@ def kv_write(kv, slot_mapping, rows):
     if rc != 0:
         raise ValueError("slot past the cache or repeated slot")
     return kvb
+
+
+def uv_proj(out, w_uv):
+    """The W_UV up-projection, fp64: y[t, h, v] = sum_c out[t, h, c] * w_uv[h, c, v].
+
+    out [T, h, 512] (float, e.g. the decode output), w_uv [h, 512, 128] as bf16 bits or a
+    bf16 tensor.  A plain contraction ("RFC: Context Parallel Modeling for DeepSeek-Style
+    Attention", 3.5: W_UV maps each head's 512-wide latent output to its value space),
+    done by numpy's einsum in float64.
+    """
+    if not isinstance(out, np.ndarray):
+        out = out.detach().cpu().double().numpy()
+    # bf16 bit patterns widen exactly: they are the top half of a float32
+    w = (_as_bf16_bits(w_uv).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.einsum("thc,hcv->thv", np.asarray(out, dtype=np.float64), w)

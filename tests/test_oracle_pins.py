@@ -414,3 +414,34 @@ def test_decode_after_write_reads_the_new_token_row():
     for hh in range(3):
         assert np.array_equal(out[1, hh], bf(new_row[0, :D_V]))
         assert lse[1, hh] == 0.0
+
+
+# --------------------------------------------------------------------------------------
+# W_UV up-projection
+# --------------------------------------------------------------------------------------
+def test_uv_proj_equals_a_plain_loop_on_a_tiny_case():
+    rng = np.random.default_rng(70)
+    out = rng.standard_normal((2, 3, D_V))
+    w_bits = bf16_bits(rng.standard_normal((3, D_V, 128)).astype(np.float32))
+    w = bits_to_f64(w_bits)
+    y = oracle.uv_proj(out, w_bits)
+    for t in range(2):
+        for hh in range(3):
+            for v in (0, 1, 77, 127):
+                acc = 0.0
+                for c in range(D_V):
+                    acc += float(out[t, hh, c]) * float(w[hh, c, v])
+                assert abs(y[t, hh, v] - acc) <= 1e-9 * (1 + abs(acc))
+
+
+def test_uv_proj_identity_weights_and_linearity():
+    rng = np.random.default_rng(71)
+    out = rng.standard_normal((4, 2, D_V))
+    eye = np.zeros((2, D_V, 128), np.float32)
+    eye[:, np.arange(128), np.arange(128)] = 1.0
+    assert np.array_equal(oracle.uv_proj(out, bf16_bits(eye)), out[:, :, :128])
+    w_bits = bf16_bits(rng.standard_normal((2, D_V, 128)).astype(np.float32))
+    a, b = rng.standard_normal((4, 2, D_V)), rng.standard_normal((4, 2, D_V))
+    lhs = oracle.uv_proj(2.0 * a - b, w_bits)
+    rhs = 2.0 * oracle.uv_proj(a, w_bits) - oracle.uv_proj(b, w_bits)
+    assert np.allclose(lhs, rhs, rtol=0, atol=1e-9)
