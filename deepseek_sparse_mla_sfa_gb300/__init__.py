@@ -22,9 +22,11 @@ D_QK = 576
 D_V = 512
 MAX_HEADS = 128
 MAX_SPLITS = 64
+BLOCK_TABLE_PER_TOKEN = 1   # sfa_decode_ex flag: one block-table row per query token
 
 __all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
-           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "SfaError", "D_QK", "D_V"]
+           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "kv_write", "uv_proj",
+           "SfaError", "D_QK", "D_V", "BLOCK_TABLE_PER_TOKEN"]
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -56,13 +58,17 @@ def workspace_bytes(B: int, Q: int, h: int, top_k: int, n_splits: int) -> int:
 
 def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int = 1, Q: int = 1,
            merge: bool = True, out=None, lse=None, out_part=None, lse_part=None, workspace=None,
-           stream=None):
-    """Sparse MLA decode (C ABI ``sfa_decode``).
+           stream=None, interleave: int = 0, block_table_per_token: bool = False):
+    """Sparse MLA decode (C ABI ``sfa_decode_ex``; ``sfa_decode`` when both layout options
+    are off).
 
     q [B*Q, h, 576] bf16, kv [num_blocks, block_size, 576] bf16, block_table [B, max_blocks]
-    int32, seq_lens [B] int32, topk_idx [B*Q, top_k] int32 (-1 = padding), all on one CUDA
-    device.  Returns (out [B*Q, h, 512] fp32, lse [B*Q, h] fp32); with n_splits > 1 and
-    merge=False returns the shard partials (out_part [n, B*Q, h, 512], lse_part [n, B*Q, h]).
+    int32 ([B*Q, max_blocks] with block_table_per_token), seq_lens [B] int32, topk_idx
+    [B*Q, top_k] int32 (-1 = padding), all on one CUDA device.  interleave = g > 0 deals the
+    cache positions to the n_splits shards g at a time (shard r holds (p // g) % n == r);
+    0 keeps contiguous shards.  Returns (out [B*Q, h, 512] fp32, lse [B*Q, h] fp32); with
+    n_splits > 1 and merge=False returns the shard partials (out_part [n, B*Q, h, 512],
+    lse_part [n, B*Q, h]).
     """
     lib = _lib.load()
     dev = q.device
@@ -77,8 +83,11 @@ def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int =
     if d != D_QK or kv.shape[2] != D_QK:
         raise ValueError("q and kv rows must have 576 columns")
     B = seq_lens.shape[0]
-    if T != B * Q or topk_idx.shape[0] != T or block_table.shape[0] != B:
+    bt_rows = T if block_table_per_token else B
+    if T != B * Q or topk_idx.shape[0] != T or block_table.shape[0] != bt_rows:
         raise ValueError("inconsistent B / Q / T")
+    if interleave < 0:
+        raise ValueError("interleave must be >= 0")
     top_k = topk_idx.shape[1]
     num_blocks, block_size = kv.shape[0], kv.shape[1]
     max_blocks = block_table.shape[1]
@@ -100,14 +109,16 @@ def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int =
     if ws_need and workspace is None:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    code = lib.sfa_decode(_ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens), _ptr(topk_idx),
-                          B, Q, h, top_k, num_blocks, block_size, max_blocks, float(scale),
-                          n_splits, _ptr(out if (n_splits == 1 or merge) else None),
-                          _ptr(lse if (n_splits == 1 or merge) else None),
-                          _ptr(out_part if n_splits > 1 else None),
-                          _ptr(lse_part if n_splits > 1 else None), _ptr(workspace), ws_bytes,
-                          _stream_ptr(stream, dev))
-    _lib.check("sfa_decode", code)
+    flags = BLOCK_TABLE_PER_TOKEN if block_table_per_token else 0
+    code = lib.sfa_decode_ex(_ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens), _ptr(topk_idx),
+                             B, Q, h, top_k, num_blocks, block_size, max_blocks, float(scale),
+                             n_splits, int(interleave), flags,
+                             _ptr(out if (n_splits == 1 or merge) else None),
+                             _ptr(lse if (n_splits == 1 or merge) else None),
+                             _ptr(out_part if n_splits > 1 else None),
+                             _ptr(lse_part if n_splits > 1 else None), _ptr(workspace), ws_bytes,
+                             _stream_ptr(stream, dev))
+    _lib.check("sfa_decode_ex", code)
     if n_splits > 1 and not merge:
         return out_part, lse_part
     return out, lse

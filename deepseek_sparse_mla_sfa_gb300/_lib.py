@@ -29,6 +29,7 @@ SZ = ctypes.c_size_t
 
 SIGNATURES = {
     "sfa_decode": ([P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, P, P, SZ, P], I),
+    "sfa_decode_ex": ([P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, P, P, P, P, P, SZ, P], I),
     "sfa_decode_workspace_bytes": ([I, I, I, I, I], SZ),
     "sfa_lse_merge": ([P, P, I, I, I, P, P, P], I),
     "sfa_decode_host_staging_bytes": ([I, I, I, I, I, I], SZ),

@@ -151,9 +151,20 @@ sfa_status sfa_decode(const void* q, const void* kv, const int32_t* block_table,
                       float scale, int n_splits, float* out, float* lse, float* out_part,
                       float* lse_part, void* workspace, size_t workspace_bytes,
                       sfa_stream stream) {
+  return sfa_decode_ex(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k, num_blocks, block_size,
+                       max_blocks_per_seq, scale, n_splits, 0, 0, out, lse, out_part, lse_part, workspace,
+                       workspace_bytes, stream);
+}
+
+sfa_status sfa_decode_ex(const void* q, const void* kv, const int32_t* block_table, const int32_t* seq_lens,
+                         const int32_t* topk_idx, int B, int Q, int h, int top_k, int num_blocks, int block_size,
+                         int max_blocks_per_seq, float scale, int n_splits, int interleave_size, int flags,
+                         float* out, float* lse, float* out_part, float* lse_part, void* workspace,
+                         size_t workspace_bytes, sfa_stream stream) {
   sfa_status st = check_decode_args(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k,
                                     num_blocks, block_size, max_blocks_per_seq, scale, n_splits);
   if (st != SFA_OK) return st;
+  if (interleave_size < 0 || (flags & ~SFA_BLOCK_TABLE_PER_TOKEN) != 0) return SFA_ERR_INVALID_ARG;
   const int T = B * Q;
   if (T == 0) return SFA_OK;
   const bool merge_after = n_splits > 1 && out && lse;
@@ -197,6 +208,8 @@ sfa_status sfa_decode(const void* q, const void* kv, const int32_t* block_table,
   p.status = status;
   const long long wl = g_wait_limit.load();
   p.wait_limit = wl > 0 ? wl : kDefaultWaitLimit;
+  p.interleave = interleave_size;
+  p.bt_per_token = (flags & SFA_BLOCK_TABLE_PER_TOKEN) ? 1 : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool tc = use_tc(h, block_size) && sfa::tc_supports_ptrs(q, kv, p.out);

@@ -33,6 +33,8 @@ struct DecodeParams {
   size_t workspace_bytes;
   int* status;            // per-device status word
   long long wait_limit;   // iteration cap of every bounded device wait
+  int interleave;         // > 0: shard r holds positions p with (p / interleave) % n_splits == r
+  int bt_per_token;       // block_table has one row per query token (else one per sequence)
 };
 
 // Record the first device-side error in the status word (never traps).
@@ -54,6 +56,30 @@ __host__ __device__ __forceinline__ void shard_bounds(int seq_len, int L, int r,
   if (u > L) u = L;
   lo = (int)(l > 0x7fffffff ? 0x7fffffff : l);
   hi = (int)(u < lo ? lo : u);
+}
+
+// The positions one work unit (token t, shard r) attends to.  Contiguous shards:
+// [lo, hi) = shard r of the sequence's cache clipped to the causal range.  Interleaved
+// shards (interleave = g > 0, as DCP deals a sequence's tokens to its ranks g at a
+// time): the whole causal range [0, L), keeping the positions p with (p / g) % n == r.
+struct ShardSel {
+  int lo, hi, g, n, r;
+  __host__ __device__ __forceinline__ bool has(int pos) const {
+    return pos >= lo && pos < hi && (g <= 0 || (pos / g) % n == r);
+  }
+};
+__host__ __device__ __forceinline__ ShardSel shard_sel(int seq_len, int L, int r, int n, int interleave) {
+  ShardSel s;
+  s.n = n;
+  s.r = r;
+  s.g = n > 1 ? interleave : 0;
+  if (s.g > 0) {
+    s.lo = 0;
+    s.hi = L > 0 ? L : 0;
+  } else {
+    shard_bounds(seq_len, L, r, n, s.lo, s.hi);
+  }
+  return s;
 }
 
 // Launchers (return the launch error, if any).

@@ -38,8 +38,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeParams p
   const int b = t / p.Q, i = t % p.Q;
   const int seq_len = p.seq_lens[b];
   const int L = seq_len - (p.Q - 1 - i);
-  int lo, hi;
-  shard_bounds(seq_len, L, r, p.n_splits, lo, hi);
+  const ShardSel sel = shard_sel(seq_len, L, r, p.n_splits, p.interleave);
+  const int bt_row = p.bt_per_token ? t : b;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int x = threadIdx.x; x < kHG * kDQK; x += blockDim.x) {
@@ -60,9 +60,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeParams p
   const int32_t* idx = p.topk_idx + (size_t)t * p.top_k;
   for (int j = warp; j < p.top_k; j += kWarps) {
     const int pos = idx[j];
-    if (pos < lo || pos >= hi || pos < 0) continue;
+    if (!sel.has(pos)) continue;
     const int blk = pos / p.block_size;
-    const int phys = blk < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + blk] : -1;
+    const int phys = blk < p.max_blocks ? p.block_table[(size_t)bt_row * p.max_blocks + blk] : -1;
     if (phys < 0 || phys >= p.num_blocks) {
       if (lane == 0) report_status(p.status, kStatusBadBlock);
       continue;

@@ -127,11 +127,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Physical cache row of selected entry `pos`, or -1 when the entry is padding for
 // this shard (or its block-table entry is invalid, which is reported).
-__device__ __forceinline__ int resolve_row(const DecodeParams& p, int b, int pos, int lo, int hi,
+__device__ __forceinline__ int resolve_row(const DecodeParams& p, int bt_row, int pos, const ShardSel& sel,
                                            bool report) {
-  if (pos < lo || pos >= hi || pos < 0) return -1;
+  if (!sel.has(pos)) return -1;
   const int blk = pos / p.block_size;
-  const int phys = blk < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + blk] : -1;
+  const int phys = blk < p.max_blocks ? p.block_table[(size_t)bt_row * p.max_blocks + blk] : -1;
   if (phys < 0 || phys >= p.num_blocks) {
     if (report) report_status(p.status, kStatusBadBlock);
     return -1;
@@ -163,8 +163,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int b = t / p.Q, qi = t % p.Q;
   const int seq_len = p.seq_lens[b];
   const int L = seq_len - (p.Q - 1 - qi);
-  int lo, hi;
-  shard_bounds(seq_len, L, r, p.n_splits, lo, hi);
+  const ShardSel sel = shard_sel(seq_len, L, r, p.n_splits, p.interleave);
+  const int bt_row = p.bt_per_token ? t : b;   // block-table row of this unit
   const int32_t* idx = p.topk_idx + (size_t)t * p.top_k;
   const long long wl = p.wait_limit;
 
@@ -227,9 +227,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const bool in = pos[k] >= lo && pos[k] < hi && pos[k] >= 0;
+        const bool in = sel.has(pos[k]);
         const int blk = in ? pos[k] / p.block_size : 0;
-        blkv[k] = in && blk < p.max_blocks ? __ldg(p.block_table + (size_t)b * p.max_blocks + blk) : -2;
+        blkv[k] = in && blk < p.max_blocks ? __ldg(p.block_table + (size_t)bt_row * p.max_blocks + blk) : -2;
         if (!in) blkv[k] = -3;
       }
 #pragma unroll
@@ -267,7 +267,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     for (int j0 = c_begin; j0 < c_end && off < kListCap; j0 += 32) {
       const int j = j0 + lane;
-      const int row = j < c_end ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
+      const int row = j < c_end ? resolve_row(p, bt_row, __ldg(idx + j), sel, false) : -1;
       const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
       const int o = off + __popc(mask & lanemask_lt());
       if (row >= 0 && o < kListCap) list_s[o] = row;
@@ -513,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int ord = 0;
         for (int j0 = 0; j0 < p.top_k; j0 += 32) {
           const int j = j0 + lane;
-          const int row = j < p.top_k ? resolve_row(p, b, __ldg(idx + j), lo, hi, false) : -1;
+          const int row = j < p.top_k ? resolve_row(p, bt_row, __ldg(idx + j), sel, false) : -1;
           const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
           const int o = ord + __popc(mask & lanemask_lt()) - seg * kListCap;
           if (row >= 0 && o >= 0 && o < kListCap && ((o % kNt) / 4) % kProducerWarps == pw) list_s[o] = row;

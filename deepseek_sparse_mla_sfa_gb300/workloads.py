@@ -187,3 +187,23 @@ def make(w, device="cuda", seed: Optional[int] = None) -> Inputs:
 def small(name: str, **overrides) -> Workload:
     """A copy of a named workload with some fields replaced (for test-sized cases)."""
     return replace(CONFIGS[name], **overrides)
+
+
+def per_token_block_table(inp: Inputs, shuffle: bool = True, seed: int = 0) -> torch.Tensor:
+    """A block table with one row per query token ([B*Q, max_blocks] int32), the layout a
+    speculative-decoding batch flattened to one row per token uses ("RFC: MsModeling 支持
+    Decode Context Parallel 仿真", 2.1.4.1).  Row t starts as its sequence's row; with
+    `shuffle` the sequence's physical blocks are dealt to its logical blocks in a fresh
+    random order per token, so that the tokens of one sequence read different cache rows
+    for the same position.  Unused entries stay -1."""
+    w = inp.w
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    bt = inp.block_table.cpu()
+    nblk = ((inp.seq_lens.cpu().to(torch.int64) + w.block_size - 1) // w.block_size).tolist()
+    rows = bt.repeat_interleave(w.Q, dim=0).clone()
+    if shuffle:
+        for t in range(w.T):
+            n = nblk[t // w.Q]
+            rows[t, :n] = bt[t // w.Q, :n][torch.randperm(n, generator=gen)]
+    return rows.contiguous().to(inp.block_table.device)

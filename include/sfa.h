@@ -128,6 +128,31 @@ sfa_status sfa_lse_merge(const float *out_part, const float *lse_part, int n_spl
                          int dv, float *out, float *lse, sfa_stream stream);
 
 /*
+ * sfa_decode_ex -- sfa_decode with the two layout options of decode context
+ * parallelism ("RFC: MsModeling 支持 Decode Context Parallel 仿真", 2.1.4.1):
+ *
+ *   interleave_size  0: shard r of n_splits is the contiguous range [r*c, (r+1)*c) of
+ *                    the sequence's cache, c = ceil(seq_lens[b] / n_splits) (as in
+ *                    sfa_decode).  g > 0: the sequence's positions are dealt to the
+ *                    shards g at a time, as cp_kv_cache_interleave_size deals them to
+ *                    the DCP ranks: shard r holds the positions p with (p / g) % n_splits
+ *                    == r.  Either way each shard is clipped to the token's causal range
+ *                    and the merged result is the same (up to rounding).
+ *   flags            SFA_BLOCK_TABLE_PER_TOKEN: block_table is [B*Q, max_blocks_per_seq],
+ *                    one row per query token (the table flattened for speculative
+ *                    decoding); otherwise [B, max_blocks_per_seq], one row per sequence.
+ *
+ * Every other argument, and the return codes, as in sfa_decode.  interleave_size < 0 or
+ * an unknown flag bit returns SFA_ERR_INVALID_ARG.
+ */
+#define SFA_BLOCK_TABLE_PER_TOKEN 1
+sfa_status sfa_decode_ex(const void *q, const void *kv, const int32_t *block_table, const int32_t *seq_lens,
+                         const int32_t *topk_idx, int B, int Q, int h, int top_k, int num_blocks, int block_size,
+                         int max_blocks_per_seq, float scale, int n_splits, int interleave_size, int flags,
+                         float *out, float *lse, float *out_part, float *lse_part, void *workspace,
+                         size_t workspace_bytes, sfa_stream stream);
+
+/*
  * sfa_kv_write -- the latent-cache write that precedes attention: each new token's
  * latent row (kv_lora_rank + qk_rope_head_dim = 576 bf16) is stored at the cache slot
  * slot_mapping[t] ("RFC: MsModeling 支持 Decode Context Parallel 仿真", 2.1.4.1:

@@ -54,8 +54,12 @@ def _bind(path: str):
     lib.sfa_oracle_decode.restype = I
     lib.sfa_oracle_decode_splits.argtypes = common + [I, P, P, I]
     lib.sfa_oracle_decode_splits.restype = I
+    lib.sfa_oracle_decode_ex.argtypes = common + [I, I, I, P, P, I]
+    lib.sfa_oracle_decode_ex.restype = I
     lib.sfa_oracle_decode_sampled.argtypes = common + [I, ctypes.c_long, P, P, P, P, P, I]
     lib.sfa_oracle_decode_sampled.restype = I
+    lib.sfa_oracle_decode_sampled_ex.argtypes = common + [I, I, I, ctypes.c_long, P, P, P, P, P, I]
+    lib.sfa_oracle_decode_sampled_ex.restype = I
     lib.sfa_oracle_merge.argtypes = [P, P, I, ctypes.c_long, I, P, P]
     lib.sfa_oracle_merge.restype = I
     lib.sfa_oracle_kv_write.argtypes = [P, ctypes.c_long, P, P, ctypes.c_long, I]
@@ -151,8 +155,12 @@ def decode_splits(prob: Problem, n_splits: int, nthreads: int = 0):
     return out, lse
 
 
-def decode_sampled(prob: Problem, tokens, heads, shards=None, n_splits: int = 1, nthreads: int = 0):
-    """Selected (token, head[, shard]) pairs: (out [n, 512], lse [n]) in float64."""
+def decode_sampled(prob: Problem, tokens, heads, shards=None, n_splits: int = 1, nthreads: int = 0,
+                   interleave: int = 0, bt_per_token: bool = False):
+    """Selected (token, head[, shard]) pairs: (out [n, 512], lse [n]) in float64.  The layout
+    options are those of decode_ex."""
+    if bt_per_token and prob.block_table.shape[0] != prob.T:
+        raise ValueError("a per-token block table has one row per query token")
     lib = _load()
     t = np.ascontiguousarray(tokens, dtype=np.int32)
     hh = np.ascontiguousarray(heads, dtype=np.int32)
@@ -160,10 +168,28 @@ def decode_sampled(prob: Problem, tokens, heads, shards=None, n_splits: int = 1,
     n = int(t.shape[0])
     out = np.zeros((n, D_V), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
-    rc = lib.sfa_oracle_decode_sampled(*prob._common(), int(n_splits), n, _ptr(t), _ptr(hh),
-                                       _ptr(r), _ptr(out), _ptr(lse), int(nthreads))
+    rc = lib.sfa_oracle_decode_sampled_ex(*prob._common(), int(n_splits), int(interleave),
+                                          int(bool(bt_per_token)), n, _ptr(t), _ptr(hh), _ptr(r),
+                                          _ptr(out), _ptr(lse), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"sfa_oracle_decode_sampled failed ({rc})")
+    return out, lse
+
+
+def decode_ex(prob: Problem, n_splits: int = 1, interleave: int = 0, bt_per_token: bool = False,
+              nthreads: int = 0):
+    """Per-shard partials with the layout options: shards dealt `interleave` positions at a
+    time (0 = contiguous shards) and a block table with one row per query token.  Returns
+    (out_part [n, T, h, 512], lse_part [n, T, h]) in float64; n_splits = 1 is unsplit."""
+    if bt_per_token and prob.block_table.shape[0] != prob.T:
+        raise ValueError("a per-token block table has one row per query token")
+    lib = _load()
+    out = np.zeros((n_splits, prob.T, prob.h, D_V), dtype=np.float64)
+    lse = np.zeros((n_splits, prob.T, prob.h), dtype=np.float64)
+    rc = lib.sfa_oracle_decode_ex(*prob._common(), int(n_splits), int(interleave), int(bool(bt_per_token)),
+                                  _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"sfa_oracle_decode_ex failed ({rc})")
     return out, lse
 
 

@@ -41,7 +41,12 @@
  *  - Indices are logical token positions; anything outside [0, L) is padding.
  *  - Query token i of Q sees positions [0, seq_lens[b] - (Q-1-i)).
  *  - Shard r of n covers positions [r*c, (r+1)*c) of the sequence's cache with
- *    c = ceil(seq_lens[b] / n), intersected with the token's causal range.
+ *    c = ceil(seq_lens[b] / n), intersected with the token's causal range.  With an
+ *    interleave size g > 0 ("cp_kv_cache_interleave_size", same page 2.1.4.1: tokens
+ *    are dealt to the DCP ranks g at a time), shard r instead holds the positions p
+ *    of the causal range with (p / g) mod n = r.
+ *  - The block table has one row per sequence, or (flattened for speculative
+ *    decoding, same page 2.1.4.1) one row per query token.
  *  - Duplicate indices count once per list entry.
  *
  * Arithmetic: bf16 inputs are widened exactly to double; every sum is a plain
@@ -73,6 +78,8 @@ typedef struct {
   const int32_t *block_table, *seq_lens, *topk_idx;
   int B, Q, h, top_k, num_blocks, block_size, max_blocks_per_seq, D, DV;
   double scale;
+  int interleave;     /* > 0: shard r holds positions p with (p / interleave) % n == r */
+  int bt_per_token;   /* block_table has one row per query token instead of per sequence */
 } problem_t;
 
 static int check_problem(const problem_t *p) {
@@ -89,25 +96,34 @@ static long causal_len(const problem_t *p, int t) {
   return (long)p->seq_lens[b] - (long)(p->Q - 1 - i);
 }
 
-/* Physical cache row of logical position pos of sequence b, or -1 when the
- * block table does not hold a valid block for it. */
-static long slot_of(const problem_t *p, int b, long pos) {
+/* Physical cache row of logical position pos through block-table row `row`, or -1
+ * when the table does not hold a valid block for it. */
+static long slot_of(const problem_t *p, int row, long pos) {
   long blk = pos / p->block_size;
   if (blk < 0 || blk >= p->max_blocks_per_seq) return -1;
-  long phys = p->block_table[(long)b * p->max_blocks_per_seq + blk];
+  long phys = p->block_table[(long)row * p->max_blocks_per_seq + blk];
   if (phys < 0 || phys >= p->num_blocks) return -1;
   return phys * p->block_size + pos % p->block_size;
 }
 
+/* Whether list entry pos belongs to the unit: inside [lo, hi) and, for shard r of n
+ * with interleaving, dealt to shard r. */
+static int in_unit(const problem_t *p, long pos, long lo, long hi, int n, int r) {
+  if (pos < lo || pos >= hi) return 0;
+  if (p->interleave > 0 && n > 1 && r >= 0) return (pos / p->interleave) % n == r;
+  return 1;
+}
+
 /*
  * Attention of token t, head hh over the selected positions that fall in
- * [lo, hi) (already clipped to the causal range by the caller).
+ * [lo, hi) (already clipped to the causal range by the caller) and, with
+ * interleaving, in shard r of n_sh.
  * out_row receives DV doubles; *lse_out the log-sum-exp.  Returns the number
  * of list entries used, or -1 if an entry points at a block the table lacks.
  */
-static long attend(const problem_t *p, int t, int hh, long lo, long hi, double *scores,
+static long attend(const problem_t *p, int t, int hh, long lo, long hi, int n_sh, int r, double *scores,
                    double *out_row, double *lse_out) {
-  int b = t / p->Q;
+  int b = p->bt_per_token ? t : t / p->Q;   /* block-table row */
   const uint16_t *qrow = p->q + ((size_t)t * p->h + hh) * p->D;
   const int32_t *idx = p->topk_idx + (size_t)t * p->top_k;
   long n = 0;
@@ -115,7 +131,7 @@ static long attend(const problem_t *p, int t, int hh, long lo, long hi, double *
   /* scores s_j = scale * <q, K_j> for every kept entry, in list order */
   for (int j = 0; j < p->top_k; ++j) {
     long pos = idx[j];
-    if (pos < lo || pos >= hi) continue;
+    if (!in_unit(p, pos, lo, hi, n_sh, r)) continue;
     long slot = slot_of(p, b, pos);
     if (slot < 0) return -1;
     const uint16_t *krow = p->kv + (size_t)slot * p->D;
@@ -135,7 +151,7 @@ static long attend(const problem_t *p, int t, int hh, long lo, long hi, double *
   long k = 0;
   for (int j = 0; j < p->top_k; ++j) {
     long pos = idx[j];
-    if (pos < lo || pos >= hi) continue;
+    if (!in_unit(p, pos, lo, hi, n_sh, r)) continue;
     long slot = slot_of(p, b, pos);
     double w = exp(scores[k++] - m);
     l += w;
@@ -181,17 +197,17 @@ static void run_item(job_t *jb, long it, double *scores) {
   }
   long L = causal_len(p, t);
   long lo = 0, hi = L;
-  if (r >= 0) {
+  int n = jb->n_splits > 0 ? jb->n_splits : 1;
+  if (r >= 0 && p->interleave <= 0) {
     /* shard r of n_splits over the sequence's cache, clipped to the causal range */
     int b = t / p->Q;
-    int n = jb->n_splits > 0 ? jb->n_splits : 1;
     long S = p->seq_lens[b];
     long c = S > 0 ? (S + n - 1) / n : 0;
     lo = (long)r * c;
     hi = (long)(r + 1) * c;
     if (hi > L) hi = L;
   }
-  if (attend(p, t, hh, lo, hi, scores, orow, lrow) < 0) jb->status = ORACLE_ERR_ARG;
+  if (attend(p, t, hh, lo, hi, n, r, scores, orow, lrow) < 0) jb->status = ORACLE_ERR_ARG;
 }
 
 static void *worker(void *arg) {
@@ -247,7 +263,7 @@ static int run_jobs(const job_t *proto, int nthreads) {
 static problem_t make_problem(const uint16_t *q, const uint16_t *kv, const int32_t *block_table,
                               const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h,
                               int top_k, int num_blocks, int block_size, int max_blocks_per_seq, int D,
-                              int DV, double scale) {
+                              int DV, double scale, int interleave, int bt_per_token) {
   problem_t p;
   p.q = q;
   p.kv = kv;
@@ -264,6 +280,8 @@ static problem_t make_problem(const uint16_t *q, const uint16_t *kv, const int32
   p.D = D;
   p.DV = DV;
   p.scale = scale;
+  p.interleave = interleave;
+  p.bt_per_token = bt_per_token;
   return p;
 }
 
@@ -275,7 +293,7 @@ int sfa_oracle_decode(const uint16_t *q, const uint16_t *kv, const int32_t *bloc
                       int num_blocks, int block_size, int max_blocks_per_seq, int D, int DV,
                       double scale, double *out, double *lse, int nthreads) {
   problem_t p = make_problem(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k, num_blocks,
-                             block_size, max_blocks_per_seq, D, DV, scale);
+                             block_size, max_blocks_per_seq, D, DV, scale, 0, 0);
   if (check_problem(&p) != ORACLE_OK || !out || !lse) return ORACLE_ERR_ARG;
   job_t jb;
   memset(&jb, 0, sizeof jb);
@@ -298,7 +316,7 @@ int sfa_oracle_decode_splits(const uint16_t *q, const uint16_t *kv, const int32_
                              int DV, double scale, int n_splits, double *out_part, double *lse_part,
                              int nthreads) {
   problem_t p = make_problem(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k, num_blocks,
-                             block_size, max_blocks_per_seq, D, DV, scale);
+                             block_size, max_blocks_per_seq, D, DV, scale, 0, 0);
   if (check_problem(&p) != ORACLE_OK || n_splits < 1 || !out_part || !lse_part) return ORACLE_ERR_ARG;
   job_t jb;
   memset(&jb, 0, sizeof jb);
@@ -311,19 +329,64 @@ int sfa_oracle_decode_splits(const uint16_t *q, const uint16_t *kv, const int32_
 }
 
 /*
+ * The two entry points above with the layout options: per-shard partials with shards
+ * interleaved `interleave` positions at a time (0 = contiguous shards), and a block
+ * table with one row per query token (bt_per_token != 0).  n_splits = 1 gives the
+ * unsplit result in out_part / lse_part.
+ */
+int sfa_oracle_decode_ex(const uint16_t *q, const uint16_t *kv, const int32_t *block_table,
+                         const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h, int top_k,
+                         int num_blocks, int block_size, int max_blocks_per_seq, int D, int DV, double scale,
+                         int n_splits, int interleave, int bt_per_token, double *out_part, double *lse_part,
+                         int nthreads) {
+  problem_t p = make_problem(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k, num_blocks,
+                             block_size, max_blocks_per_seq, D, DV, scale, interleave, bt_per_token);
+  if (check_problem(&p) != ORACLE_OK || n_splits < 1 || interleave < 0 || !out_part || !lse_part)
+    return ORACLE_ERR_ARG;
+  job_t jb;
+  memset(&jb, 0, sizeof jb);
+  jb.p = &p;
+  jb.n_splits = n_splits > 1 ? n_splits : 0;
+  jb.n_items = (long)n_splits * B * Q * h;
+  jb.out = out_part;
+  jb.lse = lse_part;
+  return run_jobs(&jb, nthreads);
+}
+
+/*
  * Selected (token, head[, shard]) pairs only, for spot checks of full-size
  * workloads.  split_r may be NULL (unsplit) or give a shard per sample, in
  * which case n_splits must be the shard count.  out [n, DV], lse [n].
  */
+int sfa_oracle_decode_sampled_ex(const uint16_t *q, const uint16_t *kv, const int32_t *block_table,
+                                 const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h,
+                                 int top_k, int num_blocks, int block_size, int max_blocks_per_seq, int D,
+                                 int DV, double scale, int n_splits, int interleave, int bt_per_token,
+                                 long n_samples, const int32_t *sample_t, const int32_t *sample_h,
+                                 const int32_t *sample_r, double *out, double *lse, int nthreads);
+
 int sfa_oracle_decode_sampled(const uint16_t *q, const uint16_t *kv, const int32_t *block_table,
                               const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h,
                               int top_k, int num_blocks, int block_size, int max_blocks_per_seq, int D,
                               int DV, double scale, int n_splits, long n_samples,
                               const int32_t *sample_t, const int32_t *sample_h,
                               const int32_t *sample_r, double *out, double *lse, int nthreads) {
+  return sfa_oracle_decode_sampled_ex(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k, num_blocks,
+                                      block_size, max_blocks_per_seq, D, DV, scale, n_splits, 0, 0, n_samples,
+                                      sample_t, sample_h, sample_r, out, lse, nthreads);
+}
+
+/* The sampled entry point with the layout options of sfa_oracle_decode_ex. */
+int sfa_oracle_decode_sampled_ex(const uint16_t *q, const uint16_t *kv, const int32_t *block_table,
+                                 const int32_t *seq_lens, const int32_t *topk_idx, int B, int Q, int h,
+                                 int top_k, int num_blocks, int block_size, int max_blocks_per_seq, int D,
+                                 int DV, double scale, int n_splits, int interleave, int bt_per_token,
+                                 long n_samples, const int32_t *sample_t, const int32_t *sample_h,
+                                 const int32_t *sample_r, double *out, double *lse, int nthreads) {
   problem_t p = make_problem(q, kv, block_table, seq_lens, topk_idx, B, Q, h, top_k, num_blocks,
-                             block_size, max_blocks_per_seq, D, DV, scale);
-  if (check_problem(&p) != ORACLE_OK || n_samples < 0 || !sample_t || !sample_h || !out || !lse)
+                             block_size, max_blocks_per_seq, D, DV, scale, interleave, bt_per_token);
+  if (check_problem(&p) != ORACLE_OK || n_samples < 0 || interleave < 0 || !sample_t || !sample_h || !out ||
+      !lse)
     return ORACLE_ERR_ARG;
   long T = (long)B * Q;
   for (long s = 0; s < n_samples; ++s) {

@@ -81,3 +81,24 @@ def test_workspace_and_staging_sizes(lib):
 def test_wait_limit_hook_roundtrip(lib):
     old = lib.sfa_set_wait_limit(123)
     assert lib.sfa_set_wait_limit(old) == 123
+
+
+def _decode_ex(lib, g, flags, **kw):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, idx=FAKE, B=2, Q=1, h=4, top_k=8, nb=4, bs=64,
+             mb=4, scale=0.07, n=2, out=FAKE, lse=FAKE, op=FAKE, lp=FAKE, ws=P0, wsb=0, stream=P0)
+    a.update(kw)
+    return lib.sfa_decode_ex(a["q"], a["kv"], a["bt"], a["sl"], a["idx"], a["B"], a["Q"], a["h"],
+                             a["top_k"], a["nb"], a["bs"], a["mb"], a["scale"], a["n"], g, flags,
+                             a["out"], a["lse"], a["op"], a["lp"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("g,flags,kw,code", [
+    (-1, 0, {}, -1),                 # negative interleave size
+    (0, 2, {}, -1),                  # unknown flag bit
+    (0, 1 << 30, {}, -1),
+    (16, 1, dict(q=P0), -1),         # the common checks still apply
+    (16, 1, dict(n=65), -2),
+    (16, 1, dict(B=0), 0),           # nothing to do
+])
+def test_decode_ex_argument_checks(lib, g, flags, kw, code):
+    assert _decode_ex(lib, g, flags, **kw) == code

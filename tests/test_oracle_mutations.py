@@ -29,8 +29,14 @@ MUTANTS = [
     ("causal_off_by_one", "return (long)p->seq_lens[b] - (long)(p->Q - 1 - i);",
      "return (long)p->seq_lens[b] - (long)(p->Q - i);",
      [pins.test_mtp_query_tokens_see_their_own_causal_range]),
+    ("interleave_group_of_block", "if (p->interleave > 0 && n > 1 && r >= 0) return (pos / p->interleave) % n == r;",
+     "if (p->interleave > 0 && n > 1 && r >= 0) return (pos / p->block_size) % n == r;",
+     [pins.test_interleaved_shard_partials_closed_form_with_zero_query]),
+    ("bt_row_per_sequence_always", "int b = p->bt_per_token ? t : t / p->Q;   /* block-table row */",
+     "int b = t / p->Q;   /* block-table row */",
+     [pins.test_block_table_per_token_reads_each_tokens_own_row]),
     ("slot_ignores_table", "return phys * p->block_size + pos % p->block_size;",
-     "return (long)b * p->max_blocks_per_seq * p->block_size + pos;",
+     "return (long)row * p->max_blocks_per_seq * p->block_size + pos;",
      [pins.test_physical_block_placement_does_not_matter]),
     ("slot_offset_swapped", "return phys * p->block_size + pos % p->block_size;",
      "return phys * p->block_size + (pos / p->block_size) % p->block_size;",
@@ -40,8 +46,8 @@ MUTANTS = [
     ("merge_weight_sign", "double w = exp(lse_part[(size_t)r * rows + x] - L);",
      "double w = exp(L - lse_part[(size_t)r * rows + x]);",
      [pins.test_merge_identity_order_and_empty_partials]),
-    ("no_dedup_semantics", "long pos = idx[j];\n    if (pos < lo || pos >= hi) continue;",
-     "long pos = idx[j];\n    if (pos < lo || pos >= hi) continue;\n    if (j > 0 && idx[j - 1] == pos) continue;",
+    ("no_dedup_semantics", "long pos = idx[j];\n    if (!in_unit(p, pos, lo, hi, n_sh, r)) continue;",
+     "long pos = idx[j];\n    if (!in_unit(p, pos, lo, hi, n_sh, r)) continue;\n    if (j > 0 && idx[j - 1] == pos) continue;",
      [pins.test_duplicate_entries_count_once_per_list_entry]),
     ("kv_write_next_slot", "for (int d = 0; d < D; ++d) kv[(size_t)s * D + d] = rows[(size_t)t * D + d];",
      "for (int d = 0; d < D; ++d) kv[(size_t)(s + 1 < num_slots ? s + 1 : s) * D + d] = rows[(size_t)t * D + d];",
@@ -51,7 +57,7 @@ MUTANTS = [
      "    const long s = slot_mapping[t];\n    if (s < 0) continue;\n    for (int d = 0; d < D; ++d)",
      "    const long s = slot_mapping[t] < 0 ? 0 : slot_mapping[t];\n    for (int d = 0; d < D; ++d)",
      [pins.test_kv_write_places_rows_skips_padding_and_leaves_the_rest]),
-    ("padding_minus_one_only", "if (pos < lo || pos >= hi) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
+    ("padding_minus_one_only", "if (!in_unit(p, pos, lo, hi, n_sh, r)) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
      "if (pos == -1) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
      [pins.test_empty_selection_gives_zero_and_minus_inf]),
 ]

@@ -445,3 +445,102 @@ def test_uv_proj_identity_weights_and_linearity():
     lhs = oracle.uv_proj(2.0 * a - b, w_bits)
     rhs = 2.0 * oracle.uv_proj(a, w_bits) - oracle.uv_proj(b, w_bits)
     assert np.allclose(lhs, rhs, rtol=0, atol=1e-9)
+
+
+# --------------------------------------------------------------------------------------
+# layout options: interleaved DCP shards, per-token block table
+# --------------------------------------------------------------------------------------
+@pytest.mark.parametrize("n_splits,g", [(2, 1), (3, 16), (4, 64), (8, 5)])
+def test_interleaved_shards_merged_equal_unsplit(n_splits, g):
+    rng = np.random.default_rng(90 + n_splits)
+    B, S, h, Q = 3, 700, 3, 2
+    dense = rng.standard_normal((B, S, D_QK)).astype(np.float32)
+    seq_lens = [700, 131, 402]
+    q = rng.standard_normal((B * Q, h, D_QK)).astype(np.float32)
+    topk = np.full((B * Q, 210), -1, np.int32)
+    for t in range(B * Q):
+        L = seq_lens[t // Q]
+        sel = rng.choice(L, size=min(L, 200), replace=False)
+        topk[t, : len(sel)] = sel
+    prob, _ = problem(dense, seq_lens, q, topk, Q=Q, perm_seed=5)
+    out, lse = oracle.decode(prob)
+    op, lp = oracle.decode_ex(prob, n_splits=n_splits, interleave=g)
+    mo, ml = oracle.merge(op, lp)
+    np.testing.assert_allclose(mo, out, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, rtol=1e-12, atol=1e-12)
+
+
+def test_interleaved_shard_partials_closed_form_with_zero_query():
+    # q = 0: shard r's partial is the mean of the selected V rows whose position p has
+    # (p // g) % n == r, and its lse is ln(count); no such row -> (0, -inf)
+    n, g, S = 3, 8, 200
+    dense = rng_normal((1, S, D_QK), 91)
+    topk = np.random.default_rng(92).permutation(S)[:77][None, :]
+    prob, _ = problem(dense, [S], np.zeros((1, 2, D_QK), np.float32), topk, perm_seed=3)
+    op, lp = oracle.decode_ex(prob, n_splits=n, interleave=g)
+    V = bf(dense[0, :, :D_V])
+    for r in range(n):
+        sel = [p for p in topk[0] if (p // g) % n == r]
+        for hh in range(2):
+            if sel:
+                assert np.allclose(op[r, 0, hh], V[sel].mean(axis=0), rtol=0, atol=1e-12)
+                assert abs(lp[r, 0, hh] - math.log(len(sel))) < 1e-12
+            else:
+                assert np.all(op[r, 0, hh] == 0) and np.isneginf(lp[r, 0, hh])
+
+
+def test_block_table_per_token_reads_each_tokens_own_row():
+    # two query tokens of one sequence (Q = 2); token 0's row points at a copy of the
+    # sequence's blocks holding different data: each token must read through its own row
+    bs, S = 16, 64
+    dense = rng_normal((2, S, D_QK), 93)               # "sequence" 0 and an alternative copy
+    pg = Paged(dense, [S, S], bs)                       # blocks of both, one table row each
+    q = rng_normal((2, 3, D_QK), 94)
+    topk = np.tile(np.arange(0, S - 1, 3, dtype=np.int32), (2, 1))
+    # per-sequence table: both tokens read sequence 0
+    per_seq = oracle.Problem(bf16_bits(q), pg.kv, pg.block_table[:1], np.array([S], np.int32), topk, 2, SCALE)
+    o_seq, l_seq = oracle.decode(per_seq)
+    # per-token table: token 0 reads the alternative copy, token 1 sequence 0
+    tok_bt = np.stack([pg.block_table[1], pg.block_table[0]])
+    per_tok = oracle.Problem(bf16_bits(q), pg.kv, tok_bt, np.array([S], np.int32), topk, 2, SCALE)
+    o_tok, l_tok = oracle.decode_ex(per_tok, bt_per_token=True)
+    assert np.array_equal(o_tok[0, 1], o_seq[1]) and np.array_equal(l_tok[0, 1], l_seq[1])
+    # token 0 through the alternative copy equals a per-sequence problem on that copy
+    alt = oracle.Problem(bf16_bits(q), pg.kv, pg.block_table[1:], np.array([S], np.int32), topk, 2, SCALE)
+    o_alt, l_alt = oracle.decode(alt)
+    assert np.array_equal(o_tok[0, 0], o_alt[0]) and not np.allclose(o_tok[0, 0], o_seq[0])
+    # identical rows for both tokens give exactly the per-sequence result
+    same = oracle.Problem(bf16_bits(q), pg.kv, np.stack([pg.block_table[0]] * 2), np.array([S], np.int32),
+                          topk, 2, SCALE)
+    o_same, l_same = oracle.decode_ex(same, bt_per_token=True)
+    assert np.array_equal(o_same[0], o_seq) and np.array_equal(l_same[0], l_seq)
+
+
+def _problem_with_per_token_table(seed):
+    # B = 2 sequences of Q = 2 tokens; each token reads its own copy of its sequence's
+    # cache (4 dense copies with different data), positions drawn causally
+    bs, S, Q = 16, 90, 2
+    dense = rng_normal((4, S, D_QK), seed)
+    pg = Paged(dense, [S] * 4, bs, perm_seed=seed + 1)
+    q = rng_normal((4, 6, D_QK), seed + 2)
+    rng = np.random.default_rng(seed + 3)
+    topk = np.full((4, 40), -1, np.int32)
+    for t in range(4):
+        L = S - (Q - 1 - t % Q)
+        topk[t, :37] = rng.choice(L, 37, replace=False)
+    return oracle.Problem(bf16_bits(q), pg.kv, pg.block_table, np.array([S, S], np.int32), topk, Q, SCALE)
+
+
+def test_sampled_layout_options_agree_with_the_whole_grid():
+    """The sampled entry point with interleaved shards and a per-token table returns the
+    same values as the whole-grid entry point for the same (shard, token, head)."""
+    prob = _problem_with_per_token_table(seed=77)
+    n, g = 3, 5
+    op, lp = oracle.decode_ex(prob, n, interleave=g, bt_per_token=True)
+    rng = np.random.default_rng(3)
+    tt = rng.integers(0, prob.T, 20).astype(np.int32)
+    hh = rng.integers(0, prob.h, 20).astype(np.int32)
+    rr = rng.integers(0, n, 20).astype(np.int32)
+    so, sl = oracle.decode_sampled(prob, tt, hh, shards=rr, n_splits=n, interleave=g, bt_per_token=True)
+    np.testing.assert_array_equal(so, op[rr, tt, hh])
+    np.testing.assert_array_equal(sl, lp[rr, tt, hh])
