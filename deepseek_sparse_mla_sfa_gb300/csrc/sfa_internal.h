@@ -67,6 +67,12 @@ struct ShardSel {
   __host__ __device__ __forceinline__ bool has(int pos) const {
     return pos >= lo && pos < hi && (g <= 0 || (pos / g) % n == r);
   }
+  // the same test with the layout fixed at compile time (kInterleaved == (g > 0)), for
+  // loops that branch on the layout once instead of once per entry
+  template <bool kInterleaved>
+  __host__ __device__ __forceinline__ bool has_fixed(int pos) const {
+    return pos >= lo && pos < hi && (!kInterleaved || (pos / g) % n == r);
+  }
 };
 __host__ __device__ __forceinline__ ShardSel shard_sel(int seq_len, int L, int r, int n, int interleave) {
   ShardSel s;

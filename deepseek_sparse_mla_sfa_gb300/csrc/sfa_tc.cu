@@ -127,9 +127,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Physical cache row of selected entry `pos`, or -1 when the entry is padding for
 // this shard (or its block-table entry is invalid, which is reported).
+template <bool kInterleaved>
 __device__ __forceinline__ int resolve_row(const DecodeParams& p, int bt_row, int pos, const ShardSel& sel,
                                            bool report) {
-  if (!sel.has(pos)) return -1;
+  if (!sel.has_fixed<kInterleaved>(pos)) return -1;
   const int blk = pos / p.block_size;
   const int phys = blk < p.max_blocks ? p.block_table[(size_t)bt_row * p.max_blocks + blk] : -1;
   if (phys < 0 || phys >= p.num_blocks) {
@@ -139,6 +140,47 @@ __device__ __forceinline__ int resolve_row(const DecodeParams& p, int bt_row, in
   return phys * p.block_size + pos % p.block_size;
 }
 
+// One lane's share of a warp's chunk [c_begin, c_end) of the selected list, 8 entries
+// per lane per round: counts the entries that resolve to a cache row of this unit and
+// leaves the last round's rows in row_r (-1 for entries that do not).  The layout of the
+// shards is a template argument so that the loop carries no per-entry branch on it.
+template <bool kInterleaved>
+__device__ __forceinline__ int resolve_chunk(const DecodeParams& p, const int32_t* idx, int c_begin, int c_end,
+                                             int lane, const ShardSel& sel, int bt_row, bool report,
+                                             int (&row_r)[8]) {
+  int cnt = 0;
+  for (int j0 = c_begin; j0 < c_end; j0 += 32 * 8) {
+    int pos[8], blkv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int j = j0 + 32 * k + lane;
+      pos[k] = j < c_end ? __ldg(idx + j) : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const bool in = sel.has_fixed<kInterleaved>(pos[k]);
+      const int blk = in ? pos[k] / p.block_size : 0;
+      blkv[k] = in && blk < p.max_blocks ? __ldg(p.block_table + (size_t)bt_row * p.max_blocks + blk) : -2;
+      if (!in) blkv[k] = -3;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      row_r[k] = -1;
+      if (blkv[k] == -3) continue;
+      if (blkv[k] < 0 || blkv[k] >= p.num_blocks) {
+        if (report) report_status(p.status, kStatusBadBlock);
+      } else {
+        ++cnt;
+        row_r[k] = blkv[k] * p.block_size + pos[k] % p.block_size;
+      }
+    }
+  }
+  return cnt;
+}
+
+// kInterleaved: the shards are interleaved (interleave size > 0 and more than one shard);
+// the layout is fixed per instantiation so that no selection test branches on it.
+template <bool kInterleaved>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_lat,
                      const __grid_constant__ CUtensorMap tmap_rope,
@@ -217,33 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int k = 0; k < 8; ++k) row_r[k] = -1;   // warps with an empty chunk write nothing
   {
-    int cnt = 0;
-    for (int j0 = c_begin; j0 < c_end; j0 += 32 * 8) {
-      int pos[8], blkv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int j = j0 + 32 * k + lane;
-        pos[k] = j < c_end ? __ldg(idx + j) : -1;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const bool in = sel.has(pos[k]);
-        const int blk = in ? pos[k] / p.block_size : 0;
-        blkv[k] = in && blk < p.max_blocks ? __ldg(p.block_table + (size_t)bt_row * p.max_blocks + blk) : -2;
-        if (!in) blkv[k] = -3;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        row_r[k] = -1;
-        if (blkv[k] == -3) continue;
-        if (blkv[k] < 0 || blkv[k] >= p.num_blocks) {
-          if (crank == 0) report_status(p.status, kStatusBadBlock);
-        } else {
-          ++cnt;
-          row_r[k] = blkv[k] * p.block_size + pos[k] % p.block_size;
-        }
-      }
-    }
+    int cnt = resolve_chunk<kInterleaved>(p, idx, c_begin, c_end, lane, sel, bt_row, crank == 0, row_r);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (lane == 0) wcount_s[warp] = cnt;
@@ -267,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     for (int j0 = c_begin; j0 < c_end && off < kListCap; j0 += 32) {
       const int j = j0 + lane;
-      const int row = j < c_end ? resolve_row(p, bt_row, __ldg(idx + j), sel, false) : -1;
+      const int row = j < c_end ? resolve_row<kInterleaved>(p, bt_row, __ldg(idx + j), sel, false) : -1;
       const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
       const int o = off + __popc(mask & lanemask_lt());
       if (row >= 0 && o < kListCap) list_s[o] = row;
@@ -513,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int ord = 0;
         for (int j0 = 0; j0 < p.top_k; j0 += 32) {
           const int j = j0 + lane;
-          const int row = j < p.top_k ? resolve_row(p, bt_row, __ldg(idx + j), sel, false) : -1;
+          const int row = j < p.top_k ? resolve_row<kInterleaved>(p, bt_row, __ldg(idx + j), sel, false) : -1;
           const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
           const int o = ord + __popc(mask & lanemask_lt()) - seg * kListCap;
           if (row >= 0 && o >= 0 && o < kListCap && ((o % kNt) / 4) % kProducerWarps == pw) list_s[o] = row;
@@ -790,15 +806,17 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
       !make_q_map(&qrope, p.q, p.h, T, tp.q_rows, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_out_map(&omap, p.out, p.h, T * p.n_splits, tp.q_rows))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
+  const bool il = p.interleave > 0 && p.n_splits > 1;
+  auto kernel = il ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  static bool attr_set[2][64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (dev >= 0 && dev < 64 && !attr_set[il][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[il][dev] = true;
   }
-  decode_tc_kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, qlat, qrope, omap, tp);
+  kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, qlat, qrope, omap, tp);
   return cudaGetLastError();
 }
 
