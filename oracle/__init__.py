@@ -15,6 +15,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from typing import Optional
 
 import numpy as np
 
@@ -64,6 +65,8 @@ def _bind(path: str):
     lib.sfa_oracle_merge.restype = I
     lib.sfa_oracle_kv_write.argtypes = [P, ctypes.c_long, P, P, ctypes.c_long, I]
     lib.sfa_oracle_kv_write.restype = I
+    lib.sfa_oracle_topk.argtypes = [P, ctypes.c_long, P, I, I, I, I, P, I]
+    lib.sfa_oracle_topk.restype = I
     return lib
 
 
@@ -242,3 +245,32 @@ def uv_proj(out, w_uv):
     # bf16 bit patterns widen exactly: they are the top half of a float32
     w = (_as_bf16_bits(w_uv).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return np.einsum("thc,hcv->thv", np.asarray(out, dtype=np.float64), w)
+
+
+def topk(scores, k: int, seq_lens=None, Q: int = 1, S: Optional[int] = None, nthreads: int = 0) -> np.ndarray:
+    """Indexer top-k selection: for each query token t = b*Q + i, the k positions p < L
+    (L = min(S, seq_lens[b] - (Q-1-i)), or S without seq_lens) with the largest scores
+    under IEEE totalOrder, equal scores taken lower position first, written in ascending
+    position and padded with -1.  scores [T, row_stride] float32 (numpy or torch)."""
+    if not isinstance(scores, np.ndarray):
+        scores = scores.detach().cpu().numpy()
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    if sc.ndim != 2:
+        raise ValueError("scores must be [T, row_stride]")
+    T, stride = int(sc.shape[0]), int(sc.shape[1])
+    S = stride if S is None else int(S)
+    sl = None if seq_lens is None else _as_i32(seq_lens)
+    if sl is not None:
+        B = int(sl.shape[0])
+        if B * Q != T:
+            raise ValueError("scores must have B*Q rows")
+    else:
+        if T % Q:
+            raise ValueError("T must be a multiple of Q")
+        B = T // Q
+    out = np.zeros((T, int(k)), dtype=np.int32)
+    bits = sc.view(np.uint32)
+    rc = _load().sfa_oracle_topk(_ptr(bits), stride, _ptr(sl), B, int(Q), S, int(k), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"sfa_oracle_topk failed ({rc})")
+    return out

@@ -474,3 +474,130 @@ int sfa_oracle_kv_write(uint16_t *kv, long num_slots, const int32_t *slot_mappin
   }
   return ORACLE_OK;
 }
+
+/*
+ * Indexer top-k selection: the list of positions each query token attends to.
+ * "vllm-ascend PR #18870 解读", 4.5: sparse attention visits only the top-2048
+ * positions the indexer chose instead of the whole history.  The pages give no
+ * formula for the indexer's scores, so the scores are an input here:
+ *
+ *   token t = b*Q + i:  L = min(S, seq_lens[b] - (Q-1-i))   (L = S without seq_lens)
+ *   candidates        = positions 0 <= p < L with scores[t, p]
+ *   order             = score under IEEE 754 totalOrder, larger first; equal bit
+ *                       patterns: lower position first
+ *   out[t, 0:n]       = the first n = min(k, L) candidates in that order, written in
+ *                       ascending position;  out[t, n:k] = -1
+ *
+ * The tie rule and the output order are readings (the pages leave both open).
+ * scores is [T, row_stride] fp32 as raw bit patterns; out is [T, k].
+ */
+typedef struct {
+  uint32_t bits;
+  int32_t pos;
+} cand_t;
+
+/* IEEE 754 totalOrder on binary32 bit patterns: the sign decides first (negatives
+ * below positives, so -0 < +0); among positives a larger magnitude field is larger,
+ * among negatives a larger magnitude field is smaller.  NaNs take their place by the
+ * same rule: +NaN above +inf, -NaN below -inf.  Returns <0, 0, >0. */
+static int total_order_cmp(uint32_t a, uint32_t b) {
+  const int neg_a = (int)(a >> 31), neg_b = (int)(b >> 31);
+  if (neg_a != neg_b) return neg_a ? -1 : 1;
+  const uint32_t ma = a & 0x7FFFFFFFu, mb = b & 0x7FFFFFFFu;
+  if (ma == mb) return 0;
+  if (!neg_a) return ma < mb ? -1 : 1;
+  return ma > mb ? -1 : 1;
+}
+
+/* qsort order of the candidates: larger score first, then lower position first */
+static int cand_before(const void *x, const void *y) {
+  const cand_t *a = (const cand_t *)x, *b = (const cand_t *)y;
+  const int c = total_order_cmp(a->bits, b->bits);
+  if (c != 0) return c > 0 ? -1 : 1;
+  return a->pos < b->pos ? -1 : (a->pos > b->pos ? 1 : 0);
+}
+
+static int pos_ascending(const void *x, const void *y) {
+  const int32_t a = *(const int32_t *)x, b = *(const int32_t *)y;
+  return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+typedef struct {
+  const uint32_t *scores;
+  long row_stride;
+  const int32_t *seq_lens;
+  int Q, S, k;
+  int32_t *out;
+  long t0, t1;
+  int status;
+} topk_job_t;
+
+static void *topk_rows(void *arg) {
+  topk_job_t *jb = (topk_job_t *)arg;
+  cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)(jb->S > 0 ? jb->S : 1));
+  int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (size_t)(jb->k > 0 ? jb->k : 1));
+  if (!c || !sel) {
+    jb->status = ORACLE_ERR_ARG;
+    free(c);
+    free(sel);
+    return NULL;
+  }
+  for (long t = jb->t0; t < jb->t1; ++t) {
+    long L = jb->S;
+    if (jb->seq_lens) {
+      const long b = t / jb->Q, i = t % jb->Q;
+      const long causal = (long)jb->seq_lens[b] - (long)(jb->Q - 1 - i);
+      if (causal < L) L = causal;
+    }
+    if (L < 0) L = 0;
+    for (long p = 0; p < L; ++p) {
+      c[p].bits = jb->scores[(size_t)t * jb->row_stride + p];
+      c[p].pos = (int32_t)p;
+    }
+    qsort(c, (size_t)L, sizeof(cand_t), cand_before);
+    const long n = L < jb->k ? L : jb->k;
+    for (long j = 0; j < n; ++j) sel[j] = c[j].pos;
+    qsort(sel, (size_t)n, sizeof(int32_t), pos_ascending);
+    int32_t *row = jb->out + (size_t)t * jb->k;
+    for (long j = 0; j < jb->k; ++j) row[j] = j < n ? sel[j] : -1;
+  }
+  free(c);
+  free(sel);
+  return NULL;
+}
+
+int sfa_oracle_topk(const uint32_t *scores, long row_stride, const int32_t *seq_lens, int B, int Q, int S, int k,
+                    int32_t *out, int nthreads) {
+  if (!scores || !out || B < 0 || Q < 1 || S < 0 || k < 1 || row_stride < S) return ORACLE_ERR_ARG;
+  const long T = (long)B * Q;
+  if (T == 0) return ORACLE_OK;
+  if (nthreads <= 0) {
+    long nc = sysconf(_SC_NPROCESSORS_ONLN);
+    nthreads = nc > 0 ? (int)nc : 1;
+  }
+  if (nthreads > T) nthreads = (int)T;
+  if (nthreads > 256) nthreads = 256;
+  topk_job_t jobs[256];
+  pthread_t th[256];
+  int started[256];
+  for (int w = 0; w < nthreads; ++w) {
+    jobs[w].scores = scores;
+    jobs[w].row_stride = row_stride;
+    jobs[w].seq_lens = seq_lens;
+    jobs[w].Q = Q;
+    jobs[w].S = S;
+    jobs[w].k = k;
+    jobs[w].out = out;
+    jobs[w].t0 = T * w / nthreads;
+    jobs[w].t1 = T * (w + 1) / nthreads;
+    jobs[w].status = ORACLE_OK;
+    started[w] = pthread_create(&th[w], NULL, topk_rows, &jobs[w]) == 0;
+    if (!started[w]) topk_rows(&jobs[w]);
+  }
+  int st = ORACLE_OK;
+  for (int w = 0; w < nthreads; ++w) {
+    if (started[w]) pthread_join(th[w], NULL);
+    if (jobs[w].status != ORACLE_OK) st = jobs[w].status;
+  }
+  return st;
+}

@@ -57,6 +57,18 @@ MUTANTS = [
      "    const long s = slot_mapping[t];\n    if (s < 0) continue;\n    for (int d = 0; d < D; ++d)",
      "    const long s = slot_mapping[t] < 0 ? 0 : slot_mapping[t];\n    for (int d = 0; d < D; ++d)",
      [pins.test_kv_write_places_rows_skips_padding_and_leaves_the_rest]),
+    ("topk_ties_higher_position_first", "return a->pos < b->pos ? -1 : (a->pos > b->pos ? 1 : 0);",
+     "return a->pos > b->pos ? -1 : (a->pos < b->pos ? 1 : 0);",
+     [pins.test_topk_ties_take_lower_positions_first]),
+    ("topk_ignores_causal_range", "if (causal < L) L = causal;", "(void)causal;",
+     [pins.test_topk_causal_range_and_short_rows]),
+    ("topk_negatives_like_positives", "  return ma > mb ? -1 : 1;\n}", "  return ma < mb ? -1 : 1;\n}",
+     [pins.test_topk_signed_zero_infinities_and_nan_follow_total_order, pins.test_topk_distinct_scores_match_numpy_sort]),
+    ("topk_signed_zeros_equal", "if (neg_a != neg_b) return neg_a ? -1 : 1;",
+     "if (neg_a != neg_b && ((a | b) & 0x7FFFFFFFu)) return neg_a ? -1 : 1;",
+     [pins.test_topk_signed_zero_infinities_and_nan_follow_total_order]),
+    ("topk_output_in_score_order", "qsort(sel, (size_t)n, sizeof(int32_t), pos_ascending);", "(void)pos_ascending;",
+     [pins.test_topk_distinct_scores_match_numpy_sort]),
     ("padding_minus_one_only", "if (!in_unit(p, pos, lo, hi, n_sh, r)) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
      "if (pos == -1) continue;\n    long slot = slot_of(p, b, pos);\n    if (slot < 0) return -1;",
      [pins.test_empty_selection_gives_zero_and_minus_inf]),

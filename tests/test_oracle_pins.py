@@ -544,3 +544,99 @@ def test_sampled_layout_options_agree_with_the_whole_grid():
     so, sl = oracle.decode_sampled(prob, tt, hh, shards=rr, n_splits=n, interleave=g, bt_per_token=True)
     np.testing.assert_array_equal(so, op[rr, tt, hh])
     np.testing.assert_array_equal(sl, lp[rr, tt, hh])
+
+
+# ---------------------------------------------------------------------------------
+# indexer top-k selection ("vllm-ascend PR #18870 解读", 4.5: sparse attention visits
+# only the top-2048 positions the indexer chose)
+
+
+def _numpy_topk_row(row, L, k):
+    """numpy's own sort: larger score first, ties lower position first (lexsort sorts by
+    the last key first), then the chosen positions in ascending order, -1 padded."""
+    pos = np.arange(L)
+    order = np.lexsort((pos, -row[:L].astype(np.float64)))
+    sel = np.sort(order[:min(k, L)])
+    return np.concatenate([sel, np.full(k - sel.size, -1)]).astype(np.int32)
+
+
+def test_topk_distinct_scores_match_numpy_sort():
+    rng = np.random.default_rng(101)
+    T, S, k = 6, 1500, 200
+    sc = rng.standard_normal((T, S)).astype(np.float32)
+    sc[T // 2:] = -np.abs(sc[T // 2:])            # rows of negative scores only
+    got = oracle.topk(sc, k)
+    for t in range(T):
+        np.testing.assert_array_equal(got[t], _numpy_topk_row(sc[t], S, k))
+        # and the selected set is exactly argpartition's (distinct values: unique answer)
+        assert set(got[t]) == set(np.argpartition(-sc[t], k)[:k])
+
+
+def test_topk_ties_take_lower_positions_first():
+    rng = np.random.default_rng(102)
+    T, S, k = 5, 700, 333
+    sc = rng.integers(-2, 3, (T, S)).astype(np.float32) * 0.5   # five values: heavy ties
+    got = oracle.topk(sc, k)
+    for t in range(T):
+        np.testing.assert_array_equal(got[t], _numpy_topk_row(sc[t], S, k))
+    # all equal: the first k positions
+    eq = np.full((2, 50), 3.25, np.float32)
+    np.testing.assert_array_equal(oracle.topk(eq, 7), np.tile(np.arange(7, dtype=np.int32), (2, 1)))
+
+
+def test_topk_signed_zero_infinities_and_nan_follow_total_order():
+    nan = np.float32(np.nan)
+    neg_nan = np.frombuffer(np.uint32(0xFFC00000).tobytes(), np.float32)[0]
+    row = np.array([[np.float32(-np.inf), nan, np.float32(np.inf), 1.0, neg_nan, -0.0, 0.0, -1.0]], np.float32)
+    # totalOrder: -NaN < -inf < -1 < -0 < +0 < 1 < +inf < +NaN
+    assert oracle.topk(row, 1).tolist() == [[1]]
+    assert oracle.topk(row, 2).tolist() == [[1, 2]]
+    assert oracle.topk(row, 3).tolist() == [[1, 2, 3]]
+    assert oracle.topk(row, 4).tolist() == [[1, 2, 3, 6]]          # +0 before -0
+    assert oracle.topk(row, 5).tolist() == [[1, 2, 3, 5, 6]]
+    assert oracle.topk(row, 6).tolist() == [[1, 2, 3, 5, 6, 7]]
+    assert oracle.topk(row, 7).tolist() == [[0, 1, 2, 3, 5, 6, 7]]  # -inf above -NaN
+    assert oracle.topk(row, 9).tolist() == [[0, 1, 2, 3, 4, 5, 6, 7, -1]]
+    # negatives: a larger magnitude is smaller
+    neg = -np.array([[3.0, 1.0, 2.0, 0.5]], np.float32)
+    assert oracle.topk(neg, 2).tolist() == [[1, 3]]
+
+
+def test_topk_causal_range_and_short_rows():
+    rng = np.random.default_rng(103)
+    B, Q, S, k = 3, 2, 300, 64
+    sc = rng.standard_normal((B * Q, S)).astype(np.float32)
+    seq_lens = np.array([300, 40, 1], np.int32)
+    got = oracle.topk(sc, k, seq_lens=seq_lens, Q=Q, S=S)
+    for t in range(B * Q):
+        L = min(S, int(seq_lens[t // Q]) - (Q - 1 - t % Q))
+        np.testing.assert_array_equal(got[t], _numpy_topk_row(sc[t], max(L, 0), k))
+    assert np.all(got[4] == -1)                       # L = 0: nothing selected
+    np.testing.assert_array_equal(got[3][:40], np.arange(40))   # L = 40 <= k: every position
+    assert np.all(got[3][40:] == -1)
+    # seq_lens above S are clipped to S; the row stride may exceed S
+    wide = np.concatenate([sc[:2], np.full((2, 20), 1e30, np.float32)], axis=1)
+    got2 = oracle.topk(wide, k, seq_lens=np.array([5000], np.int32), Q=2, S=S)
+    np.testing.assert_array_equal(got2, oracle.topk(sc[:2], k))
+
+
+def test_topk_brute_force_threshold_property():
+    """On tiny rows, every selected score is >= every unselected one (as floats), the
+    count is min(k, L), and no position repeats."""
+    rng = np.random.default_rng(104)
+    for trial in range(200):
+        S = int(rng.integers(1, 12))
+        k = int(rng.integers(1, 14))
+        row = rng.integers(-3, 4, (1, S)).astype(np.float32)
+        got = oracle.topk(row, k)[0]
+        sel = [p for p in got if p >= 0]
+        assert len(sel) == min(k, S) and len(set(sel)) == len(sel) and sel == sorted(sel)
+        rest = [p for p in range(S) if p not in sel]
+        if sel and rest:
+            assert min(row[0, sel]) >= max(row[0, rest])
+            # among the threshold value, the chosen ones are the lowest positions
+            thr = min(row[0, sel])
+            tie_sel = [p for p in sel if row[0, p] == thr]
+            tie_rest = [p for p in rest if row[0, p] == thr]
+            if tie_rest:
+                assert max(tie_sel) < min(tie_rest)
