@@ -349,7 +349,9 @@ def measure_next_rows(sfa, inp, peaks, flush):
     """The rows after the decode step at this workload's shapes, each timed alone with CUDA
     events on the launching stream (L2 scrubbed before each launch):
       kv_write - the T new tokens' latent rows scattered into the cache at their slots;
-      uv_proj  - the W_UV up-projection of the decode output (synthetic weights)."""
+      uv_proj  - the W_UV up-projection of the decode output (synthetic weights);
+      topk     - the indexer's top-k selection producing this workload's index lists from
+                 seeded N(0, 1) scores over each sequence's cache (causal range per token)."""
     w = inp.w
     dev = inp.q.device
     T, h = w.T, w.h
@@ -361,6 +363,9 @@ def measure_next_rows(sfa, inp, peaks, flush):
     out = torch.randn((T, h, 512), generator=g).to(dev) * 0.3
     w_uv = (torch.randn((h, 512, 128), generator=g) / 512 ** 0.5).to(torch.bfloat16).to(dev)
     y = torch.empty((T, h, 128), dtype=torch.bfloat16, device=dev)
+    S = int(inp.seq_lens.max())
+    scores = workloads.indexer_scores(T, S, dev, seed=w.seed + 98)
+    idx = torch.empty((T, w.top_k), dtype=torch.int32, device=dev)
 
     def timed(fn, n):
         # the L2 scrub before each call also keeps the stream busy while the host enqueues
@@ -381,18 +386,27 @@ def measure_next_rows(sfa, inp, peaks, flush):
 
     t_kv = timed(lambda: sfa.kv_write(kv_copy, slots, rows), 30)
     t_uv = timed(lambda: sfa.uv_proj(out, w_uv, y), 30)
+    t_tk = timed(lambda: sfa.topk(scores, w.top_k, seq_lens=inp.seq_lens, Q=w.Q, S=S, out=idx), 30)
     if sfa.last_device_status() != 0:
         raise RuntimeError("device status error in the next-row kernels")
     kv_bytes = T * 1152 * 2 + T * 4
     uv_bytes = T * h * 512 * 4 + h * 512 * 128 * 2 + T * h * 128 * 2
     uv_flops = 2 * T * h * 512 * 128
     uv_gbs = uv_bytes / t_uv / 1e9
+    # algorithmic bytes: each token's candidate scores read once, its list written once
+    L = (inp.seq_lens.to(torch.int64).repeat_interleave(w.Q)
+         - (w.Q - 1 - torch.arange(T, device=dev) % w.Q)).clamp(0, S)
+    tk_bytes = int(L.sum()) * 4 + T * w.top_k * 4
+    tk_gbs = tk_bytes / t_tk / 1e9
     return {
         "kv_write": {"us": t_kv * 1e6, "rows": T, "bytes": kv_bytes, "GB/s": kv_bytes / t_kv / 1e9,
                      "note": "latency-bound at this size (one 1152-byte row per warp)"},
         "uv_proj": {"us": t_uv * 1e6, "shape": f"[{T},{h},512] x [{h},512,128]", "TFLOP/s": uv_flops / t_uv / 1e12,
                     "roofline": {"bound": "hbm", "achieved": uv_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                  "frac": uv_gbs / peaks["hbm_gbs"], "bytes": uv_bytes}},
+        "topk": {"us": t_tk * 1e6, "shape": f"[{T},{S}] -> [{T},{w.top_k}]",
+                 "roofline": {"bound": "hbm", "achieved": tk_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": tk_gbs / peaks["hbm_gbs"], "bytes": tk_bytes}},
     }
 
 

@@ -25,7 +25,7 @@ MAX_SPLITS = 64
 BLOCK_TABLE_PER_TOKEN = 1   # sfa_decode_ex flag: one block-table row per query token
 
 __all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
-           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "kv_write", "uv_proj",
+           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "kv_write", "uv_proj", "topk",
            "SfaError", "D_QK", "D_V", "BLOCK_TABLE_PER_TOKEN"]
 
 
@@ -255,6 +255,42 @@ def kv_write(kv, slot_mapping, rows, stream=None):
                             _stream_ptr(stream, dev))
     _lib.check("sfa_kv_write", code)
     return kv
+
+
+def topk(scores, k: int, seq_lens=None, Q: int = 1, S: Optional[int] = None, out=None, stream=None):
+    """Indexer top-k selection (C ABI ``sfa_topk``): for each query token t = b*Q + i, the
+    positions of the k largest scores among [0, L), L = min(S, seq_lens[b] - (Q-1-i)) (S
+    without seq_lens), equal scores lower position first, in ascending position, -1 padded.
+
+    scores [B*Q, row_stride] fp32 (row_stride >= S, a multiple of 4), seq_lens [B] int32 or
+    None, out [B*Q, k] int32 (allocated when None), all on one CUDA device.  Returns out,
+    the topk_idx layout decode reads.
+    """
+    lib = _lib.load()
+    dev = scores.device
+    if dev.type != "cuda":
+        raise ValueError("topk runs on a CUDA device only")
+    _need(scores, "scores", torch.float32, dev, 2)
+    T, stride = scores.shape
+    S = stride if S is None else int(S)
+    if seq_lens is not None:
+        _need(seq_lens, "seq_lens", torch.int32, dev, 1)
+        B = seq_lens.shape[0]
+        if B * Q != T:
+            raise ValueError("scores must have B*Q rows")
+    else:
+        if T % Q:
+            raise ValueError("the number of score rows must be a multiple of Q")
+        B = T // Q
+    if out is None:
+        out = torch.empty((T, int(k)), dtype=torch.int32, device=dev)
+    _need(out, "out", torch.int32, dev, 2)
+    if tuple(out.shape) != (T, int(k)):
+        raise ValueError("out must be [B*Q, k]")
+    code = lib.sfa_topk(_ptr(scores), stride, _ptr(seq_lens), B, int(Q), S, int(k), _ptr(out),
+                        _stream_ptr(stream, dev))
+    _lib.check("sfa_topk", code)
+    return out
 
 
 def decode_launches(B, Q, h, top_k, block_size, n_splits, merge=True):

@@ -41,6 +41,7 @@ SIGNATURES = {
     "sfa_set_kernel_path": ([I], I),
     "sfa_decode_launches": ([I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)], I),
     "sfa_kv_write": ([P, ctypes.c_longlong, P, P, I, P], I),
+    "sfa_topk": ([P, ctypes.c_longlong, P, I, I, I, I, P, P], I),
     "sfa_uv_proj": ([P, P, P, I, I, P], I),
 }
 

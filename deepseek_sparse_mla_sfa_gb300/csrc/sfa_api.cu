@@ -8,6 +8,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <climits>
+
 #include "sfa.h"
 #include "sfa_internal.h"
 
@@ -361,6 +363,23 @@ sfa_status sfa_kv_write(void* kv, long long num_slots, const int32_t* slot_mappi
   int* status = status_word(dev);
   if (!status) return SFA_ERR_CUDA;
   return sfa::launch_kv_write(kv, num_slots, slot_mapping, rows, T, status, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SFA_OK
+             : SFA_ERR_CUDA;
+}
+
+static_assert(SFA_TOPK_MAX_S == sfa::kTopkMaxS, "top-k limit of the header and the kernel");
+
+sfa_status sfa_topk(const float* scores, long long row_stride, const int32_t* seq_lens, int B, int Q, int S, int k,
+                    int32_t* topk_idx, sfa_stream stream) {
+  if (B < 0 || Q < 1 || S < 0 || k < 1 || row_stride < S || row_stride % 4 != 0) return SFA_ERR_INVALID_ARG;
+  if ((long long)B * Q > INT_MAX / 8) return SFA_ERR_UNSUPPORTED;
+  if (S > sfa::kTopkMaxS) return SFA_ERR_UNSUPPORTED;
+  if (B == 0) return SFA_OK;
+  if (!topk_idx || !aligned(topk_idx, 4) || (S > 0 && (!scores || !aligned(scores, 16))) ||
+      (seq_lens && !aligned(seq_lens, 4)))
+    return SFA_ERR_INVALID_ARG;
+  return sfa::launch_topk(scores, row_stride, seq_lens, B, Q, S, k, topk_idx, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? SFA_OK
              : SFA_ERR_CUDA;

@@ -12,6 +12,8 @@ constexpr int kDQK = 576;  // kv_lora_rank + qk_rope_head_dim
 constexpr int kDV = 512;   // kv_lora_rank
 constexpr int kMaxHeads = 128;
 constexpr int kMaxSplits = 64;
+constexpr int kTopkChunkMax = 32768;                  // candidate positions one top-k CTA holds
+constexpr int kTopkMaxS = 8 * kTopkChunkMax;          // a cluster of at most 8 CTAs per token
 
 // Device status codes (mirror sfa_status values).
 constexpr int kStatusTimeout = -5;
@@ -92,6 +94,11 @@ __host__ __device__ __forceinline__ ShardSel shard_sel(int seq_len, int L, int r
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, long long wait_limit,
                            int* status, cudaStream_t stream);
+// Indexer top-k: cluster size C (CTAs per query token) and positions per CTA for T
+// tokens over S candidate positions on a GPU with n_sms SMs.
+void topk_plan(int T, int S, int n_sms, int& C, int& chunk);
+cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t* seq_lens, int B, int Q, int S,
+                        int k, int32_t* out, cudaStream_t stream);
 cudaError_t launch_kv_write(void* kv, long long num_slots, const int32_t* slot_mapping, const void* rows, int T,
                             int* status, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,

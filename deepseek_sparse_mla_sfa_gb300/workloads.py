@@ -207,3 +207,31 @@ def per_token_block_table(inp: Inputs, shuffle: bool = True, seed: int = 0) -> t
             n = nblk[t // w.Q]
             rows[t, :n] = bt[t // w.Q, :n][torch.randperm(n, generator=gen)]
     return rows.contiguous().to(inp.block_table.device)
+
+
+def indexer_scores(T: int, S: int, device="cuda", seed: int = 0, kind: str = "normal",
+                   stride: Optional[int] = None) -> torch.Tensor:
+    """Seeded stand-in for the indexer's scores, fp32 [T, stride] (stride = S rounded up to
+    a multiple of 4 unless given; columns past S hold +inf, which no selection may pick).
+    kind "normal": N(0, 1); "ties": five values {-1, -0.5, 0, 0.5, 1} (heavy ties);
+    "special": N(0, 1) with signed zeros, infinities and NaNs mixed in."""
+    device = torch.device(device)
+    stride = ((S + 3) // 4) * 4 if stride is None else int(stride)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    out = torch.full((T, stride), float("inf"), dtype=torch.float32, device=device)
+    if kind == "normal":
+        out[:, :S] = torch.randn((T, S), generator=gen, device=device)
+    elif kind == "ties":
+        out[:, :S] = torch.randint(-2, 3, (T, S), generator=gen, device=device).float() * 0.5
+    elif kind == "special":
+        x = torch.randn((T, S), generator=gen, device=device)
+        pick = torch.randint(0, 16, (T, S), generator=gen, device=device)
+        # +0, -0, +inf, -inf, +NaN (0x7FC00000) and -NaN (0xFFC00000), each 1/16 of the entries
+        specials = torch.tensor([0, -0x80000000, 0x7F800000, -0x800000, 0x7FC00000, -0x400000],
+                                dtype=torch.int32, device=device).view(torch.float32)
+        x = torch.where(pick < 6, specials[pick.clamp(max=5)], x)
+        out[:, :S] = x
+    else:
+        raise ValueError(f"unknown score kind {kind}")
+    return out

@@ -153,6 +153,32 @@ sfa_status sfa_decode_ex(const void *q, const void *kv, const int32_t *block_tab
                          size_t workspace_bytes, sfa_stream stream);
 
 /*
+ * sfa_topk -- the indexer's top-k selection: for each query token, the positions of the
+ * k largest indexer scores, the list sparse attention then visits ("vllm-ascend PR
+ * #18870 解读", 4.5: only the top-2048 positions chosen by the indexer are attended).
+ * The pages give no formula for the scores themselves; they are an input here.
+ *
+ *   scores      device fp32 [B*Q, row_stride]: row t holds the scores of positions 0..S-1
+ *               of token t's sequence (columns S..row_stride-1 are never read);
+ *               16-byte aligned, row_stride >= S and a multiple of 4
+ *   seq_lens    device int32 [B] or NULL: token t = b*Q + i chooses among the positions
+ *               [0, min(S, seq_lens[b] - (Q-1-i))) (the causal range sfa_decode uses);
+ *               NULL: among [0, S)
+ *   topk_idx    device int32 [B*Q, k], written: the chosen positions in ascending order,
+ *               then -1 where fewer than k positions are candidates -- the layout
+ *               sfa_decode reads
+ *
+ * The positions chosen are those of the k largest scores under IEEE 754 totalOrder
+ * (-0 below +0; a NaN with the sign bit clear above +inf); among equal scores the lower
+ * positions are chosen first.  1 <= k; 0 <= S <= SFA_TOPK_MAX_S.
+ * Returns SFA_OK, SFA_ERR_INVALID_ARG (bad sizes, stride, alignment or NULL buffers) or
+ * SFA_ERR_UNSUPPORTED (S above SFA_TOPK_MAX_S); nothing is launched on an error.
+ */
+#define SFA_TOPK_MAX_S 262144
+sfa_status sfa_topk(const float *scores, long long row_stride, const int32_t *seq_lens, int B, int Q, int S, int k,
+                    int32_t *topk_idx, sfa_stream stream);
+
+/*
  * sfa_kv_write -- the latent-cache write that precedes attention: each new token's
  * latent row (kv_lora_rank + qk_rope_head_dim = 576 bf16) is stored at the cache slot
  * slot_mapping[t] ("RFC: MsModeling 支持 Decode Context Parallel 仿真", 2.1.4.1:

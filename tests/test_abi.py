@@ -102,3 +102,22 @@ def _decode_ex(lib, g, flags, **kw):
 ])
 def test_decode_ex_argument_checks(lib, g, flags, kw, code):
     assert _decode_ex(lib, g, flags, **kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(), 0),                                       # B = 0: nothing to do
+    (dict(B=2, stride=6), -1),                         # row stride not a multiple of 4
+    (dict(B=2, stride=8, S=12), -1),                   # row stride below S
+    (dict(B=2, k=0), -1),
+    (dict(B=2, Q=0), -1),
+    (dict(B=-1), -1),
+    (dict(B=2, S=-1), -1),
+    (dict(B=2, S=262148, stride=262148), -2),          # above SFA_TOPK_MAX_S
+    (dict(B=2, scores=ctypes.c_void_p((1 << 20) + 4)), -1),   # scores not 16-byte aligned
+    (dict(B=2, out=P0), -1),
+    (dict(B=2, scores=P0), -1),
+])
+def test_topk_argument_checks(lib, args, code):
+    a = dict(scores=FAKE, stride=64, sl=P0, B=0, Q=1, S=64, k=8, out=FAKE)
+    a.update(args)
+    assert lib.sfa_topk(a["scores"], a["stride"], a["sl"], a["B"], a["Q"], a["S"], a["k"], a["out"], P0) == code
