@@ -94,9 +94,9 @@ __host__ __device__ __forceinline__ ShardSel shard_sel(int seq_len, int L, int r
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, long long wait_limit,
                            int* status, cudaStream_t stream);
-// Indexer top-k: cluster size C (CTAs per query token) and positions per CTA for T
-// tokens over S candidate positions on a GPU with n_sms SMs.
-void topk_plan(int T, int S, int n_sms, int& C, int& chunk);
+// Indexer top-k: cluster size C (CTAs per query token), positions per CTA and threads
+// per CTA for T tokens over S candidate positions on a GPU with n_sms SMs.
+void topk_plan(int T, int S, int n_sms, int& C, int& chunk, int& threads);
 cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t* seq_lens, int B, int Q, int S,
                         int k, int32_t* out, cudaStream_t stream);
 cudaError_t launch_kv_write(void* kv, long long num_slots, const int32_t* slot_mapping, const void* rows, int T,

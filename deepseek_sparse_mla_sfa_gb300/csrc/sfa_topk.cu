@@ -26,11 +26,12 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kTkThreads = 1024;
-constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kSlab = 4 * kTkThreads;   // positions covered by one float4 load per thread
 constexpr int kMaxBins = 2048;
 constexpr int kPasses = 3;
+// Chunks of up to kSmallChunk positions run as 512-thread CTAs (two per SM); longer
+// chunks as 1024-thread CTAs, so that a thread holds at most 32 keys.
+constexpr int kSmallThreads = 512;
+constexpr int kSmallChunk = 16 * kSmallThreads;
 
 struct TopkParams {
   const float* scores;
@@ -57,13 +58,31 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+// `n` (1, 2 or 4) consecutive words of another CTA's shared memory into v[0..n)
+__device__ __forceinline__ void ld_cluster_vec(uint32_t addr, int n, uint32_t* v) {
+  if (n == 4)
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(addr)
+                 : "memory");
+  else if (n == 2)
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr) : "memory");
+  else
+    v[0] = ld_cluster_u32(addr);
+}
 
 __device__ __forceinline__ int pass_width(int pass) { return pass < 2 ? 11 : 10; }
 
-template <int KPT>
-__global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p) {
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const TopkParams p) {
+  constexpr int kTkThreads = NT;
+  constexpr int kTkWarps = NT / 32;
+  static_assert(kTkWarps <= 32, "one warp scans the per-warp totals");
+  constexpr int kSlab = 4 * NT;                   // positions covered by one float4 load per thread
+  constexpr int kMaxPer = kMaxBins / NT;          // histogram bins per thread in the widest pass
+  static_assert(kMaxPer == 2 || kMaxPer == 4, "bins per thread load as one vector");
   constexpr int kSlabs = KPT / 4;
-  __shared__ uint32_t hist[kPasses][kMaxBins];
+  __shared__ __align__(16) uint32_t hist[kPasses][kMaxBins];   // vector loads of 1, 2 or 4 bins
   __shared__ uint32_t wtot[kSlabs][kTkWarps];   // warp totals of the packed counts
   __shared__ uint32_t slab_off[kSlabs];
   __shared__ uint32_t wsum[kTkWarps];
@@ -117,17 +136,41 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
       if (valid(e) && match) atomicAdd(&hist[pass][(key[e] >> nshift) & mask], 1u);
     }
     cluster_sync();   // every CTA's histogram of this pass is complete and visible
-    // thread tid owns bins nb-1-per*tid-u (u < per): descending bins in thread order
-    const int nb = 1 << width, per = nb / kTkThreads;
-    uint32_t c[2] = {0u, 0u};
+    // thread tid owns bins nb-1-per*tid-u (u < per): descending bins in thread order.
+    // The cluster's counts of those bins: one load per CTA, all in flight together.
+    const int nb = 1 << width, per = nb / kTkThreads;   // kMaxPer, or half of it for 10 bits
+    uint32_t c[kMaxPer];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (u >= per) break;
-      const int bin = nb - 1 - per * tid - u;
-      for (uint32_t r = 0; r < C; ++r) c[u] += ld_cluster_u32(mapa(&hist[pass][bin], r));
+    for (int u = 0; u < kMaxPer; ++u) c[u] = 0u;
+    {
+      const uint32_t* own = &hist[pass][nb - per * (tid + 1)];   // the lowest of the thread's bins
+#pragma unroll
+      for (int r0 = 0; r0 < 8; r0 += 4) {   // four CTAs' loads in flight at a time
+        uint32_t v[4][kMaxPer];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+#pragma unroll
+          for (int u = 0; u < kMaxPer; ++u) v[r][u] = 0u;
+          if (r0 + r < (int)C) ld_cluster_vec(mapa(own, (uint32_t)(r0 + r)), per, v[r]);
+        }
+        // bin nb-1-per*tid-u is word per-1-u of the vector (per is kMaxPer or half of it)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int u = 0; u < kMaxPer; ++u) {
+            if (per == kMaxPer) {
+              c[u] += v[r][kMaxPer - 1 - u];
+            } else if (u < kMaxPer / 2) {
+              c[u] += v[r][kMaxPer / 2 - 1 - u];
+            }
+          }
+      }
     }
     // exclusive block scan of the per-thread sums: keys in higher bins than this thread's
-    uint32_t s = c[0] + c[1], inc = s;
+    uint32_t s = 0;
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) s += c[u];
+    uint32_t inc = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
@@ -136,19 +179,19 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
     if (lane == 31) wsum[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-      const uint32_t x = wsum[lane];
+      const uint32_t x = lane < kTkWarps ? wsum[lane] : 0u;
       uint32_t y = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t n = __shfl_up_sync(0xffffffffu, y, o);
         if (lane >= o) y += n;
       }
-      wsum[lane] = y - x;
+      if (lane < kTkWarps) wsum[lane] = y - x;
     }
     __syncthreads();
     uint32_t above = wsum[warp] + inc - s;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < kMaxPer; ++u) {
       if (u >= per) break;
       if (above < krem && krem <= above + c[u]) {
         sel_s[0] = (uint32_t)(nb - 1 - per * tid - u);
@@ -205,14 +248,14 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
     uint32_t run = 0;
 #pragma unroll
     for (int j = 0; j < kSlabs; ++j) {
-      const uint32_t x = wtot[j][lane];
+      const uint32_t x = lane < kTkWarps ? wtot[j][lane] : 0u;
       uint32_t y = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t n = __shfl_up_sync(0xffffffffu, y, o);
         if (lane >= o) y += n;
       }
-      wtot[j][lane] = y - x;
+      if (lane < kTkWarps) wtot[j][lane] = y - x;
       if (lane == 0) slab_off[j] = run;
       run += __shfl_sync(0xffffffffu, y, 31);
     }
@@ -220,11 +263,21 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
   }
   cluster_sync();   // slab offsets, warp prefixes and every CTA's total are visible
   uint32_t gbase = 0, ebase = 0;   // keys above / equal in lower-ranked CTAs
-  for (uint32_t r = 0; r < cr; ++r) {
-    const uint32_t x = ld_cluster_u32(mapa(&cta_tot, r));
-    gbase += x >> 16;
-    ebase += x & 0xFFFFu;
+  {
+    uint32_t x[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < (int)cr) x[r] = ld_cluster_u32(mapa(&cta_tot, (uint32_t)r));
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < (int)cr) {
+        gbase += x[r] >> 16;
+        ebase += x[r] & 0xFFFFu;
+      }
   }
+  // the last read of another CTA's shared memory is done; the matching wait comes after
+  // the writes, so no CTA leaves while a peer still reads its totals
+  cluster_arrive();
   int32_t* orow = p.out + (size_t)t * p.k;
 #pragma unroll
   for (int j = 0; j < kSlabs; ++j) {
@@ -235,18 +288,20 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
       bool gt, eq;
       cls(4 * j + u, gt, eq);
       const int pos = lo + kSlab * j + 4 * tid + u;
+      // the output index is below k by construction; the bound only keeps a fault out
       if (gt) {
-        orow[g + min(q, krem)] = pos;
+        const uint32_t o = g + min(q, krem);
+        if (o < (uint32_t)p.k) orow[o] = pos;
         ++g;
       } else if (eq) {
-        if (q < krem) orow[g + q] = pos;
+        if (q < krem && g + q < (uint32_t)p.k) orow[g + q] = pos;
         ++q;
       }
     }
   }
   const int n_sel = take_all ? L : p.k;
   for (int j = n_sel + (int)cr * kTkThreads + tid; j < p.k; j += (int)C * kTkThreads) orow[j] = -1;
-  cluster_sync();   // no CTA leaves while another still reads its shared memory
+  cluster_wait();
 }
 
 int sm_count() {
@@ -261,11 +316,11 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int KPT>
+template <int NT, int KPT>
 cudaError_t launch_kpt(const TopkParams& p, int T, int C, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(T * C));
-  cfg.blockDim = dim3(kTkThreads);
+  cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -275,28 +330,30 @@ cudaError_t launch_kpt(const TopkParams& p, int T, int C, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<KPT>, p);
+  return cudaLaunchKernelEx(&cfg, topk_kernel<NT, KPT>, p);
 }
 
 }  // namespace
 
-void topk_plan(int T, int S, int n_sms, int& C, int& chunk) {
-  // up to 16K positions per CTA where 8 CTAs allow it (32 keys a thread spill registers),
-  // then more CTAs per token while the grid is smaller than the GPU
+void topk_plan(int T, int S, int n_sms, int& C, int& chunk, int& threads) {
+  // at most kSmallChunk positions per CTA where 8 CTAs per token allow it, then more CTAs
+  // per token while the grid is smaller than the GPU (chunks of at least 2048 positions)
   C = 1;
-  while (C < 8 && (long long)C * (kTopkChunkMax / 2) < S) C *= 2;
-  while (C < 8 && (long long)T * C < n_sms && (S + 2 * C - 1) / (2 * C) >= kSlab) C *= 2;
+  while (C < 8 && (long long)C * kSmallChunk < S) C *= 2;
+  while (C < 8 && (long long)T * C < n_sms && (S + 2 * C - 1) / (2 * C) >= 4 * kSmallThreads) C *= 2;
   const int per = (S + C - 1) / C;
-  chunk = ((per + kSlab - 1) / kSlab) * kSlab;
-  if (chunk < kSlab) chunk = kSlab;
+  threads = per <= kSmallChunk ? kSmallThreads : 2 * kSmallThreads;
+  const int slab = 4 * threads;
+  chunk = ((per + slab - 1) / slab) * slab;
+  if (chunk < slab) chunk = slab;
 }
 
 cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t* seq_lens, int B, int Q, int S,
                         int k, int32_t* out, cudaStream_t stream) {
   const int T = B * Q;
   if (T == 0) return cudaSuccess;
-  int C = 1, chunk = kSlab;
-  topk_plan(T, S, sm_count(), C, chunk);
+  int C = 1, chunk = 0, threads = 0;
+  topk_plan(T, S, sm_count(), C, chunk, threads);
   TopkParams p;
   p.scores = scores;
   p.row_stride = row_stride;
@@ -306,10 +363,13 @@ cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t
   p.k = k;
   p.chunk = chunk;
   p.out = out;
-  if (chunk <= 4 * kTkThreads) return launch_kpt<4>(p, T, C, stream);
-  if (chunk <= 8 * kTkThreads) return launch_kpt<8>(p, T, C, stream);
-  if (chunk <= 16 * kTkThreads) return launch_kpt<16>(p, T, C, stream);
-  return launch_kpt<32>(p, T, C, stream);
+  if (threads == kSmallThreads) {
+    if (chunk <= 4 * kSmallThreads) return launch_kpt<kSmallThreads, 4>(p, T, C, stream);
+    if (chunk <= 8 * kSmallThreads) return launch_kpt<kSmallThreads, 8>(p, T, C, stream);
+    return launch_kpt<kSmallThreads, 16>(p, T, C, stream);
+  }
+  if (chunk <= 32 * kSmallThreads) return launch_kpt<2 * kSmallThreads, 16>(p, T, C, stream);
+  return launch_kpt<2 * kSmallThreads, 32>(p, T, C, stream);
 }
 
 }  // namespace sfa
