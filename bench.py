@@ -419,12 +419,16 @@ def measure_next_rows(sfa, inp, peaks, flush):
 
 
 def read_traffic(kernel: str, tc_path: bool, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this build."""
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's sources (its
+    .cu file, the host entry points and every header) still match the capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     from deepseek_sparse_mla_sfa_gb300 import build as _b
-    src_hash = _b.source_hash()
+    src = {"decode": "sfa_tc.cu" if tc_path else "sfa_simt.cu", "lse_merge": "sfa_merge.cu"}.get(kernel)
+    if src is None:
+        return None
+    src_hash = _b.source_hash([src, "sfa_api.cu"])
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#"):

@@ -34,12 +34,16 @@ def _deps():
         sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "sfa.h")]
 
 
-def source_hash() -> str:
-    """Short hash of every CUDA source and header the library is built from."""
+def source_hash(sources=None) -> str:
+    """Short hash of the CUDA sources and headers the library is built from; with
+    `sources` (basenames of .cu files), of those sources and every header only."""
     import hashlib
     h = hashlib.sha256()
     for d in _deps():
-        h.update(os.path.basename(d).encode())
+        base = os.path.basename(d)
+        if sources is not None and base.endswith(".cu") and base not in sources:
+            continue
+        h.update(base.encode())
         with open(d, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
