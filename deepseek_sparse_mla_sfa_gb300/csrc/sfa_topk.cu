@@ -6,17 +6,20 @@
 // Order: IEEE 754 totalOrder of the fp32 scores, larger first; equal scores are taken
 // lower position first.  Output: the chosen positions in ascending order, then -1.
 //
-// One cluster of C CTAs (C = 1..8) per query token; CTA r of the cluster holds the
-// contiguous chunk [r*chunk, (r+1)*chunk) of the token's candidate range in registers,
-// as 32-bit keys whose unsigned order is the totalOrder of the scores.
-//   * Radix select in three passes (11, 11 and 10 key bits from the top).  In each pass
-//     every CTA counts its keys that still carry the chosen prefix into a shared-memory
-//     histogram; the cluster sums the histograms over distributed shared memory and every
-//     CTA finds the same bin, the one holding the k-th largest key.  A pass whose bin
-//     must be taken whole ends the search early.
-//   * Ordered compaction: per-thread counts of keys above the threshold and equal to it
-//     go through a block scan; the totals of lower-ranked CTAs of the cluster give each
-//     CTA its base; each chosen position then knows its output index.
+// One cluster of C CTAs (C = 1..8, C = 1 for rows of up to 32K positions) per query
+// token; CTA r of the cluster stages the contiguous chunk [r*chunk, (r+1)*chunk) of the
+// token's candidate range in shared memory, as 32-bit keys whose unsigned order is the
+// totalOrder of the scores.
+//   * Radix select in three passes (11, 11 and 10 key bits from the top).  Pass 0 counts
+//     every key into a shared-memory histogram; the keys that fall in the chosen bin are
+//     then copied to a short candidate list, which passes 1 and 2 scan instead of the
+//     whole chunk.  With C > 1 the cluster sums each pass's histograms over distributed
+//     shared memory, and every CTA finds the same bin.  A pass whose bin must be taken
+//     whole ends the search early.
+//   * Ordered compaction: each warp owns a contiguous run of the chunk; ballots give the
+//     order within a warp, a block scan of the warps' (above, equal) counts and the
+//     totals of lower-ranked CTAs give each warp its base, so every chosen position
+//     knows its output index and the list comes out sorted without a sort.
 // No wait in this kernel spins: the only synchronisation is block and cluster barriers.
 #include "sfa_internal.h"
 #include "sfa_ptx.cuh"
@@ -26,12 +29,21 @@ namespace {
 
 using namespace ptx;
 
+constexpr int kTkThreads = 1024;
+constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kMaxBins = 2048;
 constexpr int kPasses = 3;
-// Chunks of up to kSmallChunk positions run as 512-thread CTAs (two per SM); longer
-// chunks as 1024-thread CTAs, so that a thread holds at most 32 keys.
-constexpr int kSmallThreads = 512;
-constexpr int kSmallChunk = 16 * kSmallThreads;
+constexpr int kPer = kMaxBins / kTkThreads;   // histogram bins per thread in an 11-bit pass
+constexpr int kCandCap = 8192;                // candidates kept after pass 0 (32 KB)
+constexpr int kCandPerWarp = kCandCap / kTkWarps;
+static_assert(kPer == 2, "bin ownership below assumes two bins per thread");
+static_assert(kTopkChunkMax % (32 * kTkWarps) == 0, "a chunk splits into whole warp runs");
+
+// dynamic shared memory: keys | candidate keys | candidate positions | histograms
+__host__ __device__ constexpr int kOffCand(int chunk) { return chunk * 4; }
+__host__ __device__ constexpr int kOffCpos(int chunk) { return chunk * 4 + kCandCap * 4; }
+__host__ __device__ constexpr int kOffHist(int chunk) { return chunk * 4 + 2 * kCandCap * 4; }
+__host__ __device__ constexpr int topk_smem_bytes(int chunk) { return kOffHist(chunk) + kPasses * kMaxBins * 4; }
 
 struct TopkParams {
   const float* scores;
@@ -58,36 +70,72 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
-// `n` (1, 2 or 4) consecutive words of another CTA's shared memory into v[0..n)
-__device__ __forceinline__ void ld_cluster_vec(uint32_t addr, int n, uint32_t* v) {
-  if (n == 4)
-    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-                 : "r"(addr)
-                 : "memory");
-  else if (n == 2)
-    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr) : "memory");
-  else
-    v[0] = ld_cluster_u32(addr);
+__device__ __forceinline__ void ld_cluster_v2(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
 }
 
 __device__ __forceinline__ int pass_width(int pass) { return pass < 2 ? 11 : 10; }
 
-template <int NT, int KPT>
-__global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const TopkParams p) {
-  constexpr int kTkThreads = NT;
-  constexpr int kTkWarps = NT / 32;
-  static_assert(kTkWarps <= 32, "one warp scans the per-warp totals");
-  constexpr int kSlab = 4 * NT;                   // positions covered by one float4 load per thread
-  constexpr int kMaxPer = kMaxBins / NT;          // histogram bins per thread in the widest pass
-  static_assert(kMaxPer == 2 || kMaxPer == 4, "bins per thread load as one vector");
-  constexpr int kSlabs = KPT / 4;
-  __shared__ __align__(16) uint32_t hist[kPasses][kMaxBins];   // vector loads of 1, 2 or 4 bins
-  __shared__ uint32_t wtot[kSlabs][kTkWarps];   // warp totals of the packed counts
-  __shared__ uint32_t slab_off[kSlabs];
-  __shared__ uint32_t wsum[kTkWarps];
-  __shared__ uint32_t sel_s[3];                 // chosen bin, keys still needed, keys in the bin
-  __shared__ uint32_t cta_tot;                  // this CTA's (above << 16 | equal) total
+// Exclusive warp scan of one value per lane; also returns the warp's total.
+__device__ __forceinline__ uint32_t warp_exclusive_scan(uint32_t v, uint32_t& total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - v;
+}
+
+// Exclusive block scan of one value per thread (in thread order); also returns the total.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t x = wsum[lane];
+    uint32_t y = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += n;
+    }
+    wsum[lane] = y - x;
+    if (lane == 31) wsum[32] = y;
+  }
+  __syncthreads();
+  total = wsum[32];
+  const uint32_t r = wsum[warp] + inc - v;
+  __syncthreads();   // wsum is reused by the next scan
+  return r;
+}
+
+__global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint32_t tk_smem[];
+  uint32_t* keys = tk_smem;
+  uint32_t* cand = tk_smem + kOffCand(p.chunk) / 4;
+  uint32_t* cpos = tk_smem + kOffCpos(p.chunk) / 4;
+  uint32_t* hist = tk_smem + kOffHist(p.chunk) / 4;   // [kPasses][kMaxBins]
+  __shared__ uint32_t wsum[33];
+  __shared__ uint32_t wg_s[kTkWarps], we_s[kTkWarps];   // per-warp (above, equal) counts, then bases
+  __shared__ uint32_t sel_s[3];                         // chosen bin, keys still needed, keys in the bin
+  __shared__ uint32_t wcand_s[kTkWarps];               // candidates each warp listed
+  __shared__ uint32_t ncand_over_s;                     // some warp listed more than it keeps
+  __shared__ uint32_t cta_tot[2];                       // this CTA's (above, equal) totals
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t C = cluster_nctarank(), cr = cluster_ctarank();
@@ -101,207 +149,285 @@ __global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const TopkParams p)
   }
   const bool take_all = L <= p.k;   // every candidate is chosen: no search
   const int lo = (int)cr * p.chunk;
-  const int hi = min(lo + p.chunk, L);
+  const int n_here = max(0, min(p.chunk, L - lo));   // valid keys of this CTA: keys[0, n_here)
 
-  for (int x = tid; x < kPasses * kMaxBins; x += kTkThreads) (&hist[0][0])[x] = 0;
+  for (int x = tid; x < kPasses * kMaxBins; x += kTkThreads) hist[x] = 0u;
+  if (tid == 0) ncand_over_s = 0u;
 
-  // this thread's keys: slab j holds positions lo + kSlab*j + 4*tid + (0..3)
-  uint32_t key[KPT];
-  const float* row = p.scores + (size_t)t * p.row_stride;
+  // ---- stage the chunk: 16-byte loads, all of a thread's in flight together -----------
+  {
+    const float* row = p.scores + (size_t)t * p.row_stride + lo;
+    constexpr int kUnroll = 8;
+    for (int j0 = 4 * tid; j0 < n_here; j0 += 4 * kTkThreads * kUnroll) {
+      float4 v[kUnroll];
 #pragma unroll
-  for (int j = 0; j < kSlabs; ++j) {
-    const int base = lo + kSlab * j + 4 * tid;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (base < hi) v = __ldg(reinterpret_cast<const float4*>(row + base));
-    key[4 * j] = order_key(__float_as_uint(v.x));
-    key[4 * j + 1] = order_key(__float_as_uint(v.y));
-    key[4 * j + 2] = order_key(__float_as_uint(v.z));
-    key[4 * j + 3] = order_key(__float_as_uint(v.w));
+      for (int u = 0; u < kUnroll; ++u) {
+        const int j = j0 + 4 * kTkThreads * u;
+        v[u] = j < n_here ? __ldg(reinterpret_cast<const float4*>(row + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int j = j0 + 4 * kTkThreads * u;
+        if (j < n_here)
+          *reinterpret_cast<uint4*>(keys + j) =
+              make_uint4(order_key(__float_as_uint(v[u].x)), order_key(__float_as_uint(v[u].y)),
+                         order_key(__float_as_uint(v[u].z)), order_key(__float_as_uint(v[u].w)));
+      }
+    }
   }
-  auto valid = [&](int e) { return lo + kSlab * (e >> 2) + 4 * tid + (e & 3) < hi; };
   __syncthreads();
 
   // ---- radix select ---------------------------------------------------------------
-  uint32_t prefix = 0;   // key bits above `shift` of the k-th largest key
+  // Warp w owns keys [w*seg, (w+1)*seg) of the chunk for the sweeps that keep position
+  // order; a lane takes 4 consecutive keys of each 128-key step (one 16-byte load).
+  const int seg = p.chunk / kTkWarps;
+  const int w0 = warp * seg, w1 = min(w0 + seg, n_here);
+  uint32_t prefix = 0;               // key bits above `shift` of the k-th largest key
   int shift = 32;
-  uint32_t krem = (uint32_t)p.k;   // keys still to take at or below the prefix
+  uint32_t krem = (uint32_t)p.k;     // keys still to take at or below the prefix
+  bool use_cand = false;             // passes 1-2 scan the warps' candidate lists
+  uint32_t* my_cand = cand + warp * kCandPerWarp;
+  uint32_t* my_cpos = cpos + warp * kCandPerWarp;
 #pragma unroll 1
   for (int pass = 0; pass < kPasses && !take_all; ++pass) {
     const int width = pass_width(pass);
     const int nshift = shift - width;
     const uint32_t mask = (1u << width) - 1u;
-#pragma unroll
-    for (int e = 0; e < KPT; ++e) {
-      const bool match = pass == 0 || (key[e] >> shift) == prefix;
-      if (valid(e) && match) atomicAdd(&hist[pass][(key[e] >> nshift) & mask], 1u);
+    uint32_t* h = hist + pass * kMaxBins;
+    if (pass == 0) {
+      for (int j = 4 * tid; j < n_here; j += 4 * kTkThreads) {
+        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
+        atomicAdd(&h[v.x >> nshift], 1u);
+        if (j + 1 < n_here) atomicAdd(&h[v.y >> nshift], 1u);
+        if (j + 2 < n_here) atomicAdd(&h[v.z >> nshift], 1u);
+        if (j + 3 < n_here) atomicAdd(&h[v.w >> nshift], 1u);
+      }
+    } else if (use_cand) {
+      const int nc = (int)wcand_s[warp];
+      for (int j = lane; j < nc; j += 32) {
+        const uint32_t key = my_cand[j];
+        if ((key >> shift) == prefix) atomicAdd(&h[(key >> nshift) & mask], 1u);
+      }
+    } else {
+      for (int j = tid; j < n_here; j += kTkThreads) {
+        const uint32_t key = keys[j];
+        if ((key >> shift) == prefix) atomicAdd(&h[(key >> nshift) & mask], 1u);
+      }
     }
-    cluster_sync();   // every CTA's histogram of this pass is complete and visible
-    // thread tid owns bins nb-1-per*tid-u (u < per): descending bins in thread order.
-    // The cluster's counts of those bins: one load per CTA, all in flight together.
-    const int nb = 1 << width, per = nb / kTkThreads;   // kMaxPer, or half of it for 10 bits
-    uint32_t c[kMaxPer];
+    if (C > 1) cluster_sync(); else __syncthreads();   // this pass's histograms are complete
+    // thread tid owns bins nb-1-per*tid-u (u < per): descending bins in thread order;
+    // with C > 1 the cluster's counts of those bins, one load per CTA, all in flight
+    const int nb = 1 << width, per = nb / kTkThreads;   // 2, or 1 for the 10-bit pass
+    uint32_t c0 = 0u, c1 = 0u;   // bins nb-1-per*tid and nb-2-2*tid
+    const int lowest = nb - per * (tid + 1);
+    if (C == 1) {
+      if (per == 2) {
+        c0 = h[lowest + 1];
+        c1 = h[lowest];
+      } else {
+        c0 = h[lowest];
+      }
+    } else {
 #pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) c[u] = 0u;
-    {
-      const uint32_t* own = &hist[pass][nb - per * (tid + 1)];   // the lowest of the thread's bins
-#pragma unroll
-      for (int r0 = 0; r0 < 8; r0 += 4) {   // four CTAs' loads in flight at a time
-        uint32_t v[4][kMaxPer];
+      for (int r0 = 0; r0 < 8; r0 += 4) {
+        uint32_t va[4], vb[4];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-#pragma unroll
-          for (int u = 0; u < kMaxPer; ++u) v[r][u] = 0u;
-          if (r0 + r < (int)C) ld_cluster_vec(mapa(own, (uint32_t)(r0 + r)), per, v[r]);
-        }
-        // bin nb-1-per*tid-u is word per-1-u of the vector (per is kMaxPer or half of it)
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int u = 0; u < kMaxPer; ++u) {
-            if (per == kMaxPer) {
-              c[u] += v[r][kMaxPer - 1 - u];
-            } else if (u < kMaxPer / 2) {
-              c[u] += v[r][kMaxPer / 2 - 1 - u];
-            }
+          va[r] = vb[r] = 0u;
+          if (r0 + r < (int)C) {
+            const uint32_t a = mapa(&h[lowest], (uint32_t)(r0 + r));
+            if (per == 2)
+              ld_cluster_v2(a, va[r], vb[r]);
+            else
+              vb[r] = ld_cluster_u32(a);
           }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          c0 += vb[r];
+          c1 += va[r];
+        }
       }
+      if (per == 1) c1 = 0u;
     }
-    // exclusive block scan of the per-thread sums: keys in higher bins than this thread's
-    uint32_t s = 0;
-#pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) s += c[u];
-    uint32_t inc = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += n;
-    }
-    if (lane == 31) wsum[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-      const uint32_t x = lane < kTkWarps ? wsum[lane] : 0u;
-      uint32_t y = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t n = __shfl_up_sync(0xffffffffu, y, o);
-        if (lane >= o) y += n;
-      }
-      if (lane < kTkWarps) wsum[lane] = y - x;
-    }
-    __syncthreads();
-    uint32_t above = wsum[warp] + inc - s;
-#pragma unroll
-    for (int u = 0; u < kMaxPer; ++u) {
-      if (u >= per) break;
-      if (above < krem && krem <= above + c[u]) {
-        sel_s[0] = (uint32_t)(nb - 1 - per * tid - u);
-        sel_s[1] = krem - above;
-        sel_s[2] = c[u];
-      }
-      above += c[u];
+    uint32_t tot;
+    const uint32_t above = block_exclusive_scan(c0 + c1, wsum, tot);
+    if (above < krem && krem <= above + c0) {
+      sel_s[0] = (uint32_t)(nb - 1 - per * tid);
+      sel_s[1] = krem - above;
+      sel_s[2] = c0;
+    } else if (per == 2 && above + c0 < krem && krem <= above + c0 + c1) {
+      sel_s[0] = (uint32_t)(nb - 2 - 2 * tid);
+      sel_s[1] = krem - above - c0;
+      sel_s[2] = c1;
     }
     __syncthreads();
     prefix = (prefix << width) | sel_s[0];
     krem = sel_s[1];
     shift = nshift;
     const bool whole_bin = sel_s[2] == krem;
-    __syncthreads();   // sel_s and wsum are rewritten by the next pass
+    if (pass == 0) {
+      // each warp lists, in position order, the keys of its run whose top digit is at
+      // least the chosen bin's -- every key that can still be chosen -- with their
+      // positions.  Passes 1-2 and the output only look at these.  A warp with more than
+      // kCandPerWarp of them sends every warp back to the whole chunk.
+      uint32_t n = 0;
+      for (int j0 = w0; j0 < w1; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t key = j < w1 ? keys[j] : 0u;
+        const bool in = j < w1 && (key >> shift) >= prefix;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        const uint32_t o = n + (uint32_t)__popc(m & lanemask_lt());
+        if (in && o < (uint32_t)kCandPerWarp) {
+          my_cand[o] = key;
+          my_cpos[o] = (uint32_t)(lo + j);
+        }
+        n += (uint32_t)__popc(m);
+      }
+      if (lane == 0) wcand_s[warp] = n;
+      if (lane == 0 && n > (uint32_t)kCandPerWarp) ncand_over_s = 1u;
+      __syncthreads();
+      use_cand = ncand_over_s == 0u;
+    }
+    __syncthreads();   // sel_s is rewritten by the next pass
     if (whole_bin) break;
   }
 
   // ---- ordered compaction -----------------------------------------------------------
   // above: key bits over `shift` greater than the prefix; equal: the same bits; the
-  // first `krem` equal keys in position order are taken
-  auto cls = [&](int e, bool& gt, bool& eq) {
-    gt = false;
-    eq = false;
-    if (!valid(e)) return;
-    if (take_all) {
-      gt = true;
-      return;
+  // first `krem` equal keys in position order are taken.  With the candidate lists (in
+  // position order) the warps count from those; otherwise each warp stages its chosen
+  // and tied positions, in order, over the start of its own run of keys (a write never
+  // overtakes the reads of the same step), tagging ties in bit 31.
+  uint32_t n_st = 0, n_gt = 0, n_eq = 0;
+  if (use_cand) {
+    const uint32_t nc = wcand_s[warp];
+    for (uint32_t i0 = 0; i0 < nc; i0 += 32) {
+      const uint32_t i = i0 + lane;
+      const uint32_t kb = i < nc ? my_cand[i] >> shift : 0u;
+      n_gt += (uint32_t)__popc(__ballot_sync(0xffffffffu, i < nc && kb > prefix));
+      n_eq += (uint32_t)__popc(__ballot_sync(0xffffffffu, i < nc && kb == prefix));
     }
-    const uint32_t kb = key[e] >> shift;
-    gt = kb > prefix;
-    eq = kb == prefix;
-  };
-  uint32_t cnt[kSlabs];
+  } else {
+    for (int j0 = w0; j0 < w1; j0 += 128) {
+      const int j = j0 + 4 * lane;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (j < w1) v = *reinterpret_cast<const uint4*>(keys + j);
+      const uint32_t kv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t gbits = 0, ebits = 0;
 #pragma unroll
-  for (int j = 0; j < kSlabs; ++j) {
-    uint32_t v = 0;
+      for (int u = 0; u < 4; ++u) {
+        if (j + u >= w1) continue;
+        if (take_all) {
+          gbits |= 1u << u;
+        } else {
+          const uint32_t kb = kv[u] >> shift;
+          if (kb > prefix) gbits |= 1u << u;
+          if (kb == prefix) ebits |= 1u << u;
+        }
+      }
+      const uint32_t ng = (uint32_t)__popc(gbits), ne = (uint32_t)__popc(ebits);
+      uint32_t tot_step;
+      // packed (equal << 16 | above) counts: at most 128 of each per step
+      const uint32_t off = warp_exclusive_scan(ng | (ne << 16), tot_step);
+      uint32_t o = n_st + (off & 0xFFFFu) + (off >> 16);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      bool gt, eq;
-      cls(4 * j + u, gt, eq);
-      v += (gt ? 0x10000u : 0u) + (eq ? 1u : 0u);
+      for (int u = 0; u < 4; ++u) {
+        const bool g = gbits & (1u << u), e = ebits & (1u << u);
+        if (g || e) {
+          keys[w0 + o] = (uint32_t)(lo + j + u) | (e ? 0x80000000u : 0u);
+          ++o;
+        }
+      }
+      n_gt += tot_step & 0xFFFFu;
+      n_eq += tot_step >> 16;
+      n_st += (tot_step & 0xFFFFu) + (tot_step >> 16);
     }
-    uint32_t inc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += n;
-    }
-    if (lane == 31) wtot[j][warp] = inc;
-    cnt[j] = inc - v;   // exclusive within the warp
+  }
+  if (lane == 0) {
+    wg_s[warp] = n_gt;
+    we_s[warp] = n_eq;
   }
   __syncthreads();
   if (warp == 0) {
-    uint32_t run = 0;
+    const uint32_t xg = wg_s[lane], xe = we_s[lane];
+    uint32_t yg = xg, ye = xe;
 #pragma unroll
-    for (int j = 0; j < kSlabs; ++j) {
-      const uint32_t x = lane < kTkWarps ? wtot[j][lane] : 0u;
-      uint32_t y = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t n = __shfl_up_sync(0xffffffffu, y, o);
-        if (lane >= o) y += n;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t ng = __shfl_up_sync(0xffffffffu, yg, o), ne = __shfl_up_sync(0xffffffffu, ye, o);
+      if (lane >= o) {
+        yg += ng;
+        ye += ne;
       }
-      if (lane < kTkWarps) wtot[j][lane] = y - x;
-      if (lane == 0) slab_off[j] = run;
-      run += __shfl_sync(0xffffffffu, y, 31);
     }
-    if (lane == 0) cta_tot = run;
+    wg_s[lane] = yg - xg;
+    we_s[lane] = ye - xe;
+    if (lane == 31) {
+      cta_tot[0] = yg;
+      cta_tot[1] = ye;
+    }
   }
-  cluster_sync();   // slab offsets, warp prefixes and every CTA's total are visible
   uint32_t gbase = 0, ebase = 0;   // keys above / equal in lower-ranked CTAs
-  {
-    uint32_t x[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (r < (int)cr) x[r] = ld_cluster_u32(mapa(&cta_tot, (uint32_t)r));
+  if (C > 1) {
+    cluster_sync();   // every CTA's totals are visible
+    uint32_t xg[8], xe[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
       if (r < (int)cr) {
-        gbase += x[r] >> 16;
-        ebase += x[r] & 0xFFFFu;
+        xg[r] = ld_cluster_u32(mapa(&cta_tot[0], (uint32_t)r));
+        xe[r] = ld_cluster_u32(mapa(&cta_tot[1], (uint32_t)r));
       }
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < (int)cr) {
+        gbase += xg[r];
+        ebase += xe[r];
+      }
+    // the last read of another CTA's shared memory is done; the matching wait comes
+    // after the writes, so no CTA leaves while a peer still reads its totals
+    cluster_arrive();
+  } else {
+    __syncthreads();
   }
-  // the last read of another CTA's shared memory is done; the matching wait comes after
-  // the writes, so no CTA leaves while a peer still reads its totals
-  cluster_arrive();
+  // copy each warp's staged positions to the output: above-threshold positions all go,
+  // ties while their rank is below krem
   int32_t* orow = p.out + (size_t)t * p.k;
-#pragma unroll
-  for (int j = 0; j < kSlabs; ++j) {
-    const uint32_t b = slab_off[j] + wtot[j][warp] + cnt[j];
-    uint32_t g = gbase + (b >> 16), q = ebase + (b & 0xFFFFu);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      bool gt, eq;
-      cls(4 * j + u, gt, eq);
-      const int pos = lo + kSlab * j + 4 * tid + u;
-      // the output index is below k by construction; the bound only keeps a fault out
-      if (gt) {
-        const uint32_t o = g + min(q, krem);
-        if (o < (uint32_t)p.k) orow[o] = pos;
-        ++g;
-      } else if (eq) {
-        if (q < krem && g + q < (uint32_t)p.k) orow[g + q] = pos;
-        ++q;
+  {
+    uint32_t g = gbase + wg_s[warp], q = ebase + we_s[warp];
+    const uint32_t n_items = use_cand ? wcand_s[warp] : n_st;
+    for (uint32_t i0 = 0; i0 < n_items; i0 += 32) {
+      const uint32_t i = i0 + lane;
+      bool e, gsel;
+      uint32_t item;
+      if (use_cand) {
+        const uint32_t kb = i < n_items ? my_cand[i] >> shift : 0u;
+        gsel = i < n_items && kb > prefix;
+        e = i < n_items && kb == prefix;
+        item = i < n_items ? my_cpos[i] : 0u;
+      } else {
+        item = i < n_items ? keys[w0 + i] : 0u;
+        e = i < n_items && (item >> 31);
+        gsel = i < n_items && !(item >> 31);
       }
+      const unsigned mg = __ballot_sync(0xffffffffu, gsel), me = __ballot_sync(0xffffffffu, e);
+      const uint32_t lt = lanemask_lt();
+      const uint32_t gb = g + (uint32_t)__popc(mg & lt), eb = q + (uint32_t)__popc(me & lt);
+      const int32_t pos = (int32_t)(item & 0x7FFFFFFFu);
+      // the output index is below k by construction; the bound only keeps a fault out
+      if (gsel) {
+        const uint32_t o = gb + min(eb, krem);
+        if (o < (uint32_t)p.k) orow[o] = pos;
+      } else if (e && eb < krem) {
+        const uint32_t o = gb + eb;
+        if (o < (uint32_t)p.k) orow[o] = pos;
+      }
+      g += __popc(mg);
+      q += __popc(me);
     }
   }
   const int n_sel = take_all ? L : p.k;
   for (int j = n_sel + (int)cr * kTkThreads + tid; j < p.k; j += (int)C * kTkThreads) orow[j] = -1;
-  cluster_wait();
+  if (C > 1) cluster_wait();
 }
 
 int sm_count() {
@@ -316,36 +442,20 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int NT, int KPT>
-cudaError_t launch_kpt(const TopkParams& p, int T, int C, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(T * C));
-  cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_kernel<NT, KPT>, p);
-}
-
 }  // namespace
 
 void topk_plan(int T, int S, int n_sms, int& C, int& chunk, int& threads) {
-  // at most kSmallChunk positions per CTA where 8 CTAs per token allow it, then more CTAs
-  // per token while the grid is smaller than the GPU (chunks of at least 2048 positions)
-  C = 1;
-  while (C < 8 && (long long)C * kSmallChunk < S) C *= 2;
-  while (C < 8 && (long long)T * C < n_sms && (S + 2 * C - 1) / (2 * C) >= 4 * kSmallThreads) C *= 2;
+  // as few CTAs per token as hold the row (32K positions each), doubled while the grid
+  // would fill less than half of the GPU and the chunks stay at least 4K positions
+  C = (S + kTopkChunkMax - 1) / kTopkChunkMax;
+  if (C < 1) C = 1;
+  if (C > 8) C = 8;
+  while (C < 8 && 2LL * T * C <= n_sms && (S + 2 * C - 1) / (2 * C) >= 4096) C *= 2;
   const int per = (S + C - 1) / C;
-  threads = per <= kSmallChunk ? kSmallThreads : 2 * kSmallThreads;
-  const int slab = 4 * threads;
-  chunk = ((per + slab - 1) / slab) * slab;
-  if (chunk < slab) chunk = slab;
+  const int unit = 32 * kTkWarps;
+  chunk = ((per + unit - 1) / unit) * unit;
+  if (chunk < unit) chunk = unit;
+  threads = kTkThreads;
 }
 
 cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t* seq_lens, int B, int Q, int S,
@@ -363,13 +473,28 @@ cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t
   p.k = k;
   p.chunk = chunk;
   p.out = out;
-  if (threads == kSmallThreads) {
-    if (chunk <= 4 * kSmallThreads) return launch_kpt<kSmallThreads, 4>(p, T, C, stream);
-    if (chunk <= 8 * kSmallThreads) return launch_kpt<kSmallThreads, 8>(p, T, C, stream);
-    return launch_kpt<kSmallThreads, 16>(p, T, C, stream);
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         topk_smem_bytes(kTopkChunkMax));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
   }
-  if (chunk <= 32 * kSmallThreads) return launch_kpt<2 * kSmallThreads, 16>(p, T, C, stream);
-  return launch_kpt<2 * kSmallThreads, 32>(p, T, C, stream);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(T * C));
+  cfg.blockDim = dim3(kTkThreads);
+  cfg.dynamicSmemBytes = (size_t)topk_smem_bytes(chunk);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
 }
 
 }  // namespace sfa
