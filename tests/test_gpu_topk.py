@@ -105,3 +105,18 @@ def test_topk_lists_drive_decode_to_the_oracle():
     prob = oracle.Problem(inp.q, inp.kv, inp.block_table, inp.seq_lens, ref_idx, w.Q, w.scale)
     ref_out, ref_lse = oracle.decode(prob)
     compare(out, lse, ref_out, ref_lse, "top-k -> decode")
+
+
+@pytest.mark.parametrize("kind", ["ties", "all_equal"])
+def test_full_chunks_with_heavy_ties(kind):
+    """Rows held by one CTA each (enough tokens to fill the GPU), where so many keys tie at
+    the threshold that the per-warp candidate lists overflow and the kernel falls back to
+    sweeping the whole chunk; all-equal rows take the first k positions."""
+    T, S, k = 160, 32768, 2048
+    if kind == "ties":
+        sc = workloads.indexer_scores(T, S, "cuda", seed=21, kind="ties")
+    else:
+        sc = torch.full((T, S), 0.25, dtype=torch.float32, device="cuda")
+    g = _check(sc, k, S=S, what=kind)
+    if kind == "all_equal":
+        assert np.array_equal(g, np.tile(np.arange(k, dtype=np.int32), (T, 1)))
