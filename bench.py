@@ -217,7 +217,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = workloads.CONFIGS[args.config]
-    inp = workloads.make(w, device="cuda")
+    inp = workloads.make(w, device="cuda" if torch.cuda.is_available() else "cpu")
     acc = accounting(inp)
     per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -230,6 +230,8 @@ def run_reference(args, world, rank):
         tot += el
         line_cb = cb
     value = statistics.mean(vals) if vals else 0.0
+    if line_cb is not None:
+        line_cb = dict(line_cb, value=value)   # this run's own value, over all its steps
     line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / max(1, args.steps), "higher_is_better": True,
@@ -481,7 +483,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
-                    help="skip timing the kv_write / uv_proj rows after the decode step")
+                    help="skip timing the kv_write / uv_proj / topk rows around the decode step")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's B (smaller cases for profiler captures)")
     args = ap.parse_args()
@@ -492,12 +494,14 @@ def main():
                                 name=f"{args.config}_b{args.batch}")
         workloads.CONFIGS[w.name] = w
         args.config = w.name
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle: rank 0 alone runs it, the other ranks exit
+        # without work, and no GPU or process group is needed
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
     world, rank, local = dist_setup()
     try:
-        if args.impl == "reference":
-            run_reference(args, world, rank)
-        else:
-            run_ours(args, world, rank, local)
+        run_ours(args, world, rank, local)
     finally:
         if world > 1:
             import torch.distributed as dist
