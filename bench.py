@@ -57,7 +57,7 @@ def hold_device(cycles: int = 200_000):
 
 
 def accounting(inp: workloads.Inputs):
-    """Algorithmic work of one step: FLOPs and bytes per kernel (SURVEY-style accounting:
+    """Algorithmic work of one step: FLOPs and bytes per kernel (the method's own work:
     only the selected rows count; softmax exponentials are not FLOPs)."""
     w = inp.w
     T, h, n = w.T, w.h, w.n_splits
