@@ -25,7 +25,7 @@ MAX_SPLITS = 64
 BLOCK_TABLE_PER_TOKEN = 1   # sfa_decode_ex flag: one block-table row per query token
 
 __all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
-           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "kv_write", "uv_proj", "topk",
+           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "kv_write", "uv_proj", "topk", "HostPlan",
            "SfaError", "D_QK", "D_V", "BLOCK_TABLE_PER_TOKEN"]
 
 
@@ -209,6 +209,60 @@ def decode_host(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, scal
                                staging.numel() * staging.element_size(), _stream_ptr(stream, dev))
     _lib.check("sfa_decode_host", code)
     return out_host, lse_host
+
+
+class HostPlan:
+    """One decode_host step captured once as a CUDA graph (C ABI ``sfa_host_plan_*``), for a
+    serving loop that reuses its buffers: ``launch()`` enqueues the whole step (input copies,
+    kernels, result copies) with one graph launch.
+
+    Arguments as decode_host; the host tensors must be pinned.  Every launch reads the host
+    inputs as they are at that moment and writes out_host / lse_host; refill the inputs in
+    place between launches and synchronise before reading the results.  The tensors are kept
+    alive by the plan.  ``close()`` (or garbage collection) releases it.
+    """
+
+    def __init__(self, q_host, kv, block_table_host, seq_lens_host, topk_idx_host, scale, n_splits, Q,
+                 out_host, lse_host, staging):
+        lib = _lib.load()
+        dev = kv.device
+        _need(kv, "kv", torch.bfloat16, dev, 3)
+        for t, name, dt in ((q_host, "q_host", torch.bfloat16), (block_table_host, "block_table_host", torch.int32),
+                            (seq_lens_host, "seq_lens_host", torch.int32),
+                            (topk_idx_host, "topk_idx_host", torch.int32),
+                            (out_host, "out_host", torch.float32), (lse_host, "lse_host", torch.float32)):
+            _need(t, name, dt, torch.device("cpu"))
+            if not t.is_pinned():
+                raise ValueError(f"{name} must be pinned host memory")
+        self._keep = (q_host, kv, block_table_host, seq_lens_host, topk_idx_host, out_host, lse_host, staging)
+        self._dev = dev
+        T, h, _ = q_host.shape
+        B = seq_lens_host.shape[0]
+        top_k = topk_idx_host.shape[1]
+        plan = ctypes.c_void_p(0)
+        code = lib.sfa_host_plan_create(_ptr(q_host), _ptr(kv), _ptr(block_table_host), _ptr(seq_lens_host),
+                                        _ptr(topk_idx_host), B, Q, h, top_k, kv.shape[0], kv.shape[1],
+                                        block_table_host.shape[1], float(scale), n_splits, _ptr(out_host),
+                                        _ptr(lse_host), _ptr(staging), staging.numel() * staging.element_size(),
+                                        ctypes.byref(plan))
+        _lib.check("sfa_host_plan_create", code)
+        self._plan = plan
+
+    def launch(self, stream=None):
+        if not self._plan:
+            raise ValueError("the plan is closed")
+        _lib.check("sfa_host_plan_launch", _lib.load().sfa_host_plan_launch(self._plan, _stream_ptr(stream, self._dev)))
+
+    def close(self):
+        if getattr(self, "_plan", None):
+            _lib.load().sfa_host_plan_destroy(self._plan)
+            self._plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def uv_proj(out, w_uv, y=None, stream=None):

@@ -42,6 +42,9 @@ SIGNATURES = {
     "sfa_decode_launches": ([I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)], I),
     "sfa_kv_write": ([P, ctypes.c_longlong, P, P, I, P], I),
     "sfa_topk": ([P, ctypes.c_longlong, P, I, I, I, I, P, P], I),
+    "sfa_host_plan_create": ([P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P, SZ, P], I),
+    "sfa_host_plan_launch": ([P, P], I),
+    "sfa_host_plan_destroy": ([P], None),
     "sfa_uv_proj": ([P, P, P, I, I, P], I),
 }
 

@@ -91,6 +91,12 @@ sfa_status check_decode_args(const void* q, const void* kv, const int32_t* block
 
 }  // namespace
 
+// A captured sfa_decode_host step (see include/sfa.h).
+struct sfa_host_plan_s {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
 extern "C" {
 
 const char* sfa_status_string(sfa_status s) {
@@ -243,21 +249,33 @@ size_t sfa_decode_host_staging_bytes(int B, int Q, int h, int top_k, int max_blo
   return n;
 }
 
+// The argument checks of sfa_decode_host (SFA_OK also for an empty batch).
+static sfa_status check_host_args(const void* q_host, const void* kv, const int32_t* block_table_host,
+                                  const int32_t* seq_lens_host, const int32_t* topk_idx_host, int B, int Q, int h,
+                                  int top_k, int num_blocks, int block_size, int max_blocks_per_seq, float scale,
+                                  int n_splits, const float* out_host, const float* lse_host, const void* staging,
+                                  size_t staging_bytes) {
+  const sfa_status st = check_decode_args(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, B, Q, h,
+                                          top_k, num_blocks, block_size, max_blocks_per_seq, scale, n_splits);
+  if (st != SFA_OK || (long long)B * Q == 0) return st;
+  if (!out_host || !lse_host) return SFA_ERR_INVALID_ARG;
+  const size_t need = sfa_decode_host_staging_bytes(B, Q, h, top_k, max_blocks_per_seq, n_splits);
+  if (!staging || staging_bytes < need || !aligned(staging, 256)) return SFA_ERR_WORKSPACE;
+  return SFA_OK;
+}
+
 sfa_status sfa_decode_host(const void* q_host, const void* kv, const int32_t* block_table_host,
                            const int32_t* seq_lens_host, const int32_t* topk_idx_host, int B,
                            int Q, int h, int top_k, int num_blocks, int block_size,
                            int max_blocks_per_seq, float scale, int n_splits, float* out_host,
                            float* lse_host, void* staging, size_t staging_bytes,
                            sfa_stream stream) {
-  sfa_status st = check_decode_args(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, B,
-                                    Q, h, top_k, num_blocks, block_size, max_blocks_per_seq, scale,
-                                    n_splits);
+  sfa_status st = check_host_args(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, B, Q, h, top_k,
+                                  num_blocks, block_size, max_blocks_per_seq, scale, n_splits, out_host, lse_host,
+                                  staging, staging_bytes);
   if (st != SFA_OK) return st;
   const size_t T = (size_t)B * Q;
   if (T == 0) return SFA_OK;
-  if (!out_host || !lse_host) return SFA_ERR_INVALID_ARG;
-  const size_t need = sfa_decode_host_staging_bytes(B, Q, h, top_k, max_blocks_per_seq, n_splits);
-  if (!staging || staging_bytes < need || !aligned(staging, 256)) return SFA_ERR_WORKSPACE;
 
   char* base = static_cast<char*>(staging);
   size_t off = 0;
@@ -335,6 +353,60 @@ sfa_status sfa_decode_host(const void* q_host, const void* kv, const int32_t* bl
   }
   if (cudaMemcpyAsync(lse_host, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SFA_ERR_CUDA;
   return SFA_OK;
+}
+
+sfa_status sfa_host_plan_create(const void* q_host, const void* kv, const int32_t* block_table_host,
+                                const int32_t* seq_lens_host, const int32_t* topk_idx_host, int B, int Q, int h,
+                                int top_k, int num_blocks, int block_size, int max_blocks_per_seq, float scale,
+                                int n_splits, float* out_host, float* lse_host, void* staging,
+                                size_t staging_bytes, sfa_host_plan* plan) {
+  if (!plan) return SFA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const sfa_status chk = check_host_args(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, B, Q, h,
+                                         top_k, num_blocks, block_size, max_blocks_per_seq, scale, n_splits,
+                                         out_host, lse_host, staging, staging_bytes);
+  if (chk != SFA_OK) return chk;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
+  // everything that is set up once per device happens here, outside the capture
+  if (!status_word(dev)) return SFA_ERR_CUDA;
+  host_pipe(dev);
+  if (sfa::prepare_decode_tc() != cudaSuccess || sfa::prepare_decode_simt() != cudaSuccess) return SFA_ERR_CUDA;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return SFA_ERR_CUDA;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return SFA_ERR_CUDA;
+  }
+  const sfa_status st = sfa_decode_host(q_host, kv, block_table_host, seq_lens_host, topk_idx_host, B, Q, h, top_k,
+                                        num_blocks, block_size, max_blocks_per_seq, scale, n_splits, out_host,
+                                        lse_host, staging, staging_bytes, cs);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+  cudaStreamDestroy(cs);
+  if (st != SFA_OK || ce != cudaSuccess || !graph) {
+    if (graph) cudaGraphDestroy(graph);
+    return st != SFA_OK ? st : SFA_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return SFA_ERR_CUDA;
+  }
+  *plan = new sfa_host_plan_s{graph, exec};
+  return SFA_OK;
+}
+
+sfa_status sfa_host_plan_launch(sfa_host_plan plan, sfa_stream stream) {
+  if (!plan) return SFA_ERR_INVALID_ARG;
+  return cudaGraphLaunch(plan->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SFA_OK : SFA_ERR_CUDA;
+}
+
+void sfa_host_plan_destroy(sfa_host_plan plan) {
+  if (!plan) return;
+  cudaGraphExecDestroy(plan->exec);
+  cudaGraphDestroy(plan->graph);
+  delete plan;
 }
 
 sfa_status sfa_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, sfa_stream stream) {

@@ -92,6 +92,10 @@ __host__ __device__ __forceinline__ ShardSel shard_sel(int seq_len, int L, int r
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+// One-time per-device kernel attributes (shared-memory size), set outside any stream
+// capture; the launchers call them too.
+cudaError_t prepare_decode_simt();
+cudaError_t prepare_decode_tc();
 cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, long long wait_limit,
                            int* status, cudaStream_t stream);
 // Indexer top-k: cluster size C (CTAs per query token), positions per CTA and threads

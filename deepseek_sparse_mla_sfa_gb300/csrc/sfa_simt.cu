@@ -135,19 +135,27 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeParams p
 
 }  // namespace
 
-cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
-  const int T = p.B * p.Q;
-  if (T == 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * (kHG * kDQK + kWarps * kHG * kDV + 2 * kWarps * kHG);
+constexpr size_t kSmemSimt = sizeof(float) * (kHG * kDQK + kWarps * kHG * kDV + 2 * kWarps * kHG);
+
+cudaError_t prepare_decode_simt() {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemSimt);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
+  const int T = p.B * p.Q;
+  if (T == 0) return cudaSuccess;
+  const size_t smem = kSmemSimt;
+  cudaError_t e = prepare_decode_simt();
+  if (e != cudaSuccess) return e;
   dim3 grid(T, p.n_splits, (p.h + kHG - 1) / kHG);
   decode_simt_kernel<<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();

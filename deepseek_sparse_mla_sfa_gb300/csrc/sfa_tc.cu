@@ -789,6 +789,20 @@ int tc_launches(int T, int h, int top_k, int n_splits) {
   return 1;
 }
 
+cudaError_t prepare_decode_tc() {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    for (auto kernel : {decode_tc_kernel<false>, decode_tc_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
+    attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   const long long T = (long long)p.B * p.Q;
   const long long units = T * p.n_splits;
@@ -808,14 +822,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const bool il = p.interleave > 0 && p.n_splits > 1;
   auto kernel = il ? decode_tc_kernel<true> : decode_tc_kernel<false>;
-  static bool attr_set[2][64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[il][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[il][dev] = true;
-  }
+  cudaError_t e = prepare_decode_tc();
+  if (e != cudaSuccess) return e;
   kernel<<<(unsigned)(2 * units), kThreads, kSmemBytes, stream>>>(lat, rope, qlat, qrope, omap, tp);
   return cudaGetLastError();
 }

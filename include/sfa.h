@@ -247,6 +247,34 @@ sfa_status sfa_decode_host(const void *q_host, const void *kv, const int32_t *bl
                            sfa_stream stream);
 
 /*
+ * sfa_host_plan -- one sfa_decode_host step captured as a CUDA graph, for a serving loop
+ * that calls it with the same buffers every step: the ~20 copies, launches and stream
+ * joins of a step then cost one graph launch on the host instead of being enqueued one
+ * by one (the host side of a step otherwise takes longer than the copy engines need).
+ *
+ *   sfa_host_plan_create  records the step exactly as sfa_decode_host with the same
+ *                         arguments would enqueue it (same checks and return codes; nothing
+ *                         runs).  The host buffers must be page-locked (pinned); a failed
+ *                         capture returns SFA_ERR_CUDA and a NULL `plan` SFA_ERR_INVALID_ARG;
+ *                         *plan is NULL unless SFA_OK.  The plan keeps the pointers: every launch copies q,
+ *                         block_table, seq_lens and topk_idx in from those host buffers as
+ *                         they are at that moment and writes out and lse back to theirs, so
+ *                         the caller refills the inputs between launches.  The buffers must
+ *                         outlive the plan; staging must not be used by anything else while
+ *                         a launch may be in flight.
+ *   sfa_host_plan_launch  enqueues one step on `stream` (asynchronous, like sfa_decode_host).
+ *   sfa_host_plan_destroy releases the plan (NULL is ignored); no launch may be in flight.
+ */
+typedef struct sfa_host_plan_s *sfa_host_plan;
+sfa_status sfa_host_plan_create(const void *q_host, const void *kv, const int32_t *block_table_host,
+                                const int32_t *seq_lens_host, const int32_t *topk_idx_host, int B, int Q, int h,
+                                int top_k, int num_blocks, int block_size, int max_blocks_per_seq, float scale,
+                                int n_splits, float *out_host, float *lse_host, void *staging,
+                                size_t staging_bytes, sfa_host_plan *plan);
+sfa_status sfa_host_plan_launch(sfa_host_plan plan, sfa_stream stream);
+void sfa_host_plan_destroy(sfa_host_plan plan);
+
+/*
  * sfa_last_device_status -- synchronises `stream`, then returns and clears the
  * current device's status word: SFA_OK, SFA_ERR_DEVICE_TIMEOUT (a bounded wait
  * inside a kernel gave up; that kernel's outputs are undefined) or

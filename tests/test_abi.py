@@ -121,3 +121,14 @@ def test_topk_argument_checks(lib, args, code):
     a = dict(scores=FAKE, stride=64, sl=P0, B=0, Q=1, S=64, k=8, out=FAKE)
     a.update(args)
     assert lib.sfa_topk(a["scores"], a["stride"], a["sl"], a["B"], a["Q"], a["S"], a["k"], a["out"], P0) == code
+
+
+def test_host_plan_argument_checks(lib):
+    plan = ctypes.c_void_p(0)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 2, 1, 4, 8, 4, 64, 4, 0.07, 1, FAKE, FAKE, FAKE, 1 << 30]
+    assert lib.sfa_host_plan_create(*args, None) == -1                    # no place for the plan
+    bad = list(args)
+    bad[5] = -1                                                            # B < 0
+    assert lib.sfa_host_plan_create(*bad, ctypes.byref(plan)) == -1 and not plan.value
+    assert lib.sfa_host_plan_launch(None, P0) == -1
+    lib.sfa_host_plan_destroy(None)                                        # ignored

@@ -283,3 +283,39 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     out, lse = run_cuda(inp)
     compare(out, lse, ro, rl, "after timeout")
     assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("B,n_splits", [(4, 1), (64, 1), (8, 2)])
+def test_host_plan_replays_the_host_step(B, n_splits):
+    """The captured host step (CUDA graph) gives what decode_host gives, bit for bit, and
+    every launch reads the host inputs as they are then: refilled inputs give the
+    refilled problem's result.  B=64 takes the grouped path (4 helper streams)."""
+    w = W("plan", B=B, Q=1, h=128, S=4096, top_k=512, n_splits=n_splits, index_kind="uniform", seed=29)
+    a = workloads.make(w, device="cuda")
+    b = workloads.make(w, device="cuda", seed=30)
+    pin = lambda t: t.cpu().contiguous().pin_memory()
+    q_h, bt_h, sl_h, idx_h = pin(a.q), pin(a.block_table), pin(a.seq_lens), pin(a.topk_idx)
+    out_h = torch.empty((w.T, w.h, 512), dtype=torch.float32).pin_memory()
+    lse_h = torch.empty((w.T, w.h), dtype=torch.float32).pin_memory()
+    nbytes = sfa.decode_host_staging_bytes(w.B, w.Q, w.h, w.top_k, a.max_blocks, w.n_splits)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    plan = sfa.HostPlan(q_h, a.kv, bt_h, sl_h, idx_h, w.scale, w.n_splits, w.Q, out_h, lse_h, staging)
+    plan.launch()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = run_cuda(a)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref_out.cpu()) and torch.equal(lse_h, ref_lse.cpu())
+    # the next step: new queries and index lists in the same pinned buffers (same cache)
+    q_h.copy_(b.q.cpu())
+    idx_h.copy_(b.topk_idx.cpu())
+    plan.launch()
+    torch.cuda.synchronize()
+    nxt_out, nxt_lse = sfa.decode(b.q, a.kv, a.block_table, a.seq_lens, b.topk_idx, w.scale, n_splits=w.n_splits)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, nxt_out.cpu()) and torch.equal(lse_h, nxt_lse.cpu())
+    prob = oracle.Problem(b.q, a.kv, a.block_table, a.seq_lens, b.topk_idx, w.Q, w.scale)
+    tt, hh = sample_pairs(w.T, w.h, 8, seed=3)
+    r_out, r_lse = oracle.decode_sampled(prob, tt, hh)
+    compare(out_h[tt, hh].double().numpy(), lse_h[tt, hh].double().numpy(), r_out, r_lse, "plan, second step")
+    plan.close()
+    assert sfa.last_device_status() == 0
