@@ -36,6 +36,10 @@ SMALL = [
     W("h65_spare", B=2, Q=1, h=65, S=640, top_k=640, n_splits=1, index_kind="uniform", spare_blocks=5, seed=16),
     # more valid entries than the tcgen05 kernel keeps resolved at once (2048): list refills
     W("h128_k3000", B=1, Q=1, h=128, S=4096, top_k=3000, n_splits=1, index_kind="uniform", seed=17),
+    # the largest shard count: 64 shards of 64 positions, many of them empty
+    W("h128_n64", B=2, Q=1, h=128, S=4096, top_k=700, n_splits=64, index_kind="uniform", seed=18),
+    # a single selected position per token
+    W("h128_k1", B=3, Q=1, h=128, S=1000, top_k=1, n_splits=1, index_kind="uniform", seed=19),
 ]
 
 
