@@ -8,6 +8,7 @@
 // definition of "RFC: MsModeling 支持 Decode Context Parallel 仿真" 2.1.4.2 /
 // "vllm-ascend PR #18870 解读" 4.5 (softmax(q K^T scale) V over the selected rows
 // of the paged latent cache, with the per-head log-sum-exp).
+#include <atomic>
 #include "sfa_internal.h"
 
 namespace sfa {
@@ -138,14 +139,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_simt_kernel(DecodeParams p
 constexpr size_t kSmemSimt = sizeof(float) * (kHG * kDQK + kWarps * kHG * kDV + 2 * kWarps * kHG);
 
 cudaError_t prepare_decode_simt() {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // per device: set once (a repeat is harmless)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemSimt);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }

@@ -31,6 +31,7 @@
 // partial scores to the peer as soon as QK^T has produced them (warp w serves TMEM
 // lane quadrant w % 4).  Every wait is bounded; a wait that gives up records
 // SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
+#include <atomic>
 #include <cuda.h>
 #include <string.h>
 
@@ -790,15 +791,15 @@ int tc_launches(int T, int h, int top_k, int n_splits) {
 }
 
 cudaError_t prepare_decode_tc() {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // per device: set once (a repeat is harmless)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     for (auto kernel : {decode_tc_kernel<false>, decode_tc_kernel<true>}) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
       if (e != cudaSuccess) return e;
     }
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }

@@ -21,6 +21,7 @@
 //     totals of lower-ranked CTAs give each warp its base, so every chosen position
 //     knows its output index and the list comes out sorted without a sort.
 // No wait in this kernel spins: the only synchronisation is block and cluster barriers.
+#include <atomic>
 #include "sfa_internal.h"
 #include "sfa_ptx.cuh"
 
@@ -431,15 +432,15 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
 }
 
 int sm_count() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];   // per device, 0 until first asked
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace
@@ -473,14 +474,14 @@ cudaError_t launch_topk(const float* scores, long long row_stride, const int32_t
   p.k = k;
   p.chunk = chunk;
   p.out = out;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // per device: set once (a repeat is harmless)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          topk_smem_bytes(kTopkChunkMax));
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(T * C));

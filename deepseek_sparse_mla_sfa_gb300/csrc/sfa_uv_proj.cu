@@ -11,6 +11,7 @@
 //   K = 512              (32 MMAs of K = 16, fp32 accumulation in TMEM),
 // and writes y in bf16.  Every wait is bounded; a wait that gives up records
 // SFA_ERR_DEVICE_TIMEOUT and the CTA skips its stores.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -184,13 +185,13 @@ cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, i
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];   // per device: set once (a repeat is harmless)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(uv_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemUV);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   const dim3 grid((unsigned)((T + kTok - 1) / kTok), (unsigned)h);
   uv_proj_kernel<<<grid, kThreadsUV, kSmemUV, stream>>>(wmap, out, static_cast<__nv_bfloat16*>(y), T, h, wait_limit,
