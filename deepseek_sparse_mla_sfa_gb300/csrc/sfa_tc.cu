@@ -202,7 +202,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = crank ^ 1u;
   const int unit = blockIdx.x >> 1;
   const int T = p.B * p.Q;
-  const int t = unit % T, r = unit / T;
+  // Units go out last shard first: a sequence's most recent positions, where a sparse
+  // selection usually concentrates, are its last shard, so the heaviest units start in
+  // the first wave and the light ones fill in behind them.
+  const int t = unit % T, r = p.n_splits - 1 - unit / T;
   const int b = t / p.Q, qi = t % p.Q;
   const int seq_len = p.seq_lens[b];
   const int L = seq_len - (p.Q - 1 - qi);
