@@ -173,6 +173,26 @@ def job_value(flops_per_rank: float, ms: float, world: int) -> float:
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
+def cpu_model() -> str:
+    """The host CPU's model name, as the kernel reports it (empty when unknown)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip().lower() in ("model name", "cpu model", "hardware") and val.strip():
+                    return val.strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return ""
+
+
 def cpu_oracle_leg(inp, acc, target_s=15.0, max_tokens=None):
     """Time the fp64 oracle, as it stands, on the host cores over a bounded sample of
     the workload (whole tokens, all heads, all shards).  Returns (line dict, elapsed)."""
@@ -207,7 +227,7 @@ def cpu_oracle_leg(inp, acc, target_s=15.0, max_tokens=None):
     el = run(tokens)
     flops = FLOPS_PER_ROW_HEAD * w.h * int(kval[tokens].sum())
     val = flops / el / 1e12
-    return {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{len(tokens)} of {w.T} query tokens of {w.name}, all {w.h} heads"
                       f"{', all %d shards + merge' % w.n_splits if w.n_splits > 1 else ''}; "
                       f"{el:.2f} s fp64 on {cores} host threads"}, el
@@ -330,7 +350,8 @@ def run_ours(args, world, rank, local):
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "median_ms_per_step": statistics.median(step_ms),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Q": w.Q, "h": w.h, "S": w.S, "top_k": w.top_k,
                    "n_splits": n, "block_size": w.block_size, "seed": w.seed,
