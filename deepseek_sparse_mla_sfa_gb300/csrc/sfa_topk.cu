@@ -155,24 +155,34 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
   for (int x = tid; x < kPasses * kMaxBins; x += kTkThreads) hist[x] = 0u;
   if (tid == 0) ncand_over_s = 0u;
 
-  // ---- stage the chunk: 16-byte loads, all of a thread's in flight together -----------
+  // ---- stage the chunk and count pass 0 --------------------------------------------
+  // A chunk is at most 32 keys a thread: all of a thread's 16-byte loads are in flight
+  // at once, and each key is counted into the pass-0 histogram (top 11 bits) as it is
+  // converted and stored.
   {
+    static_assert(kTopkChunkMax <= 4 * kTkThreads * 8, "one round of 8 loads covers a chunk");
     const float* row = p.scores + (size_t)t * p.row_stride + lo;
     constexpr int kUnroll = 8;
-    for (int j0 = 4 * tid; j0 < n_here; j0 += 4 * kTkThreads * kUnroll) {
-      float4 v[kUnroll];
+    float4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int j = j0 + 4 * kTkThreads * u;
-        v[u] = j < n_here ? __ldg(reinterpret_cast<const float4*>(row + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = 4 * tid + 4 * kTkThreads * u;
+      v[u] = j < n_here ? __ldg(reinterpret_cast<const float4*>(row + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();   // the histograms are zeroed before any count lands
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int j = j0 + 4 * kTkThreads * u;
-        if (j < n_here)
-          *reinterpret_cast<uint4*>(keys + j) =
-              make_uint4(order_key(__float_as_uint(v[u].x)), order_key(__float_as_uint(v[u].y)),
-                         order_key(__float_as_uint(v[u].z)), order_key(__float_as_uint(v[u].w)));
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = 4 * tid + 4 * kTkThreads * u;
+      if (j < n_here) {
+        const uint4 kv = make_uint4(order_key(__float_as_uint(v[u].x)), order_key(__float_as_uint(v[u].y)),
+                                    order_key(__float_as_uint(v[u].z)), order_key(__float_as_uint(v[u].w)));
+        *reinterpret_cast<uint4*>(keys + j) = kv;
+        if (!take_all) {
+          atomicAdd(&hist[kv.x >> 21], 1u);
+          if (j + 1 < n_here) atomicAdd(&hist[kv.y >> 21], 1u);
+          if (j + 2 < n_here) atomicAdd(&hist[kv.z >> 21], 1u);
+          if (j + 3 < n_here) atomicAdd(&hist[kv.w >> 21], 1u);
+        }
       }
     }
   }
@@ -196,13 +206,7 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_kernel(const TopkParams p)
     const uint32_t mask = (1u << width) - 1u;
     uint32_t* h = hist + pass * kMaxBins;
     if (pass == 0) {
-      for (int j = 4 * tid; j < n_here; j += 4 * kTkThreads) {
-        const uint4 v = *reinterpret_cast<const uint4*>(keys + j);
-        atomicAdd(&h[v.x >> nshift], 1u);
-        if (j + 1 < n_here) atomicAdd(&h[v.y >> nshift], 1u);
-        if (j + 2 < n_here) atomicAdd(&h[v.z >> nshift], 1u);
-        if (j + 3 < n_here) atomicAdd(&h[v.w >> nshift], 1u);
-      }
+      // counted while staging (top 11 bits: nshift == 21)
     } else if (use_cand) {
       const int nc = (int)wcand_s[warp];
       for (int j = lane; j < nc; j += 32) {
