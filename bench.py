@@ -381,7 +381,9 @@ def measure_next_rows(sfa, inp, peaks, flush):
       kv_write - the T new tokens' latent rows scattered into the cache at their slots;
       uv_proj  - the W_UV up-projection of the decode output (synthetic weights);
       topk     - the indexer's top-k selection producing this workload's index lists from
-                 seeded N(0, 1) scores over each sequence's cache (causal range per token)."""
+                 seeded N(0, 1) scores over each sequence's cache (causal range per token);
+      lse_merge - the shard merge at the 8-shard long-context shape (8 x 32 tokens x 128
+                 heads of fp32 partials), which a single-shard step does not run."""
     w = inp.w
     dev = inp.q.device
     T, h = w.T, w.h
@@ -418,6 +420,13 @@ def measure_next_rows(sfa, inp, peaks, flush):
     t_kv = timed(lambda: sfa.kv_write(kv_copy, slots, rows), 30)
     t_uv = timed(lambda: sfa.uv_proj(out, w_uv, y), 30)
     t_tk = timed(lambda: sfa.topk(scores, w.top_k, seq_lens=inp.seq_lens, Q=w.Q, S=S, out=idx), 30)
+    lw = workloads.CONFIGS["long_dcp"]
+    m_rows = lw.T * lw.h
+    op = torch.randn((lw.n_splits, lw.T, lw.h, 512), generator=g).to(dev)
+    lp = (torch.randn((lw.n_splits, lw.T, lw.h), generator=g) * 3.0).to(dev)
+    mo = torch.empty((lw.T, lw.h, 512), dtype=torch.float32, device=dev)
+    ml = torch.empty((lw.T, lw.h), dtype=torch.float32, device=dev)
+    t_mg = timed(lambda: sfa.lse_merge(op, lp, out=mo, lse=ml), 30)
     if sfa.last_device_status() != 0:
         raise RuntimeError("device status error in the next-row kernels")
     kv_bytes = T * 1152 * 2 + T * 4
@@ -429,6 +438,8 @@ def measure_next_rows(sfa, inp, peaks, flush):
          - (w.Q - 1 - torch.arange(T, device=dev) % w.Q)).clamp(0, S)
     tk_bytes = int(L.sum()) * 4 + T * w.top_k * 4
     tk_gbs = tk_bytes / t_tk / 1e9
+    mg_bytes = (lw.n_splits + 1) * m_rows * 513 * 4
+    mg_gbs = mg_bytes / t_mg / 1e9
     return {
         "kv_write": {"us": t_kv * 1e6, "rows": T, "bytes": kv_bytes, "GB/s": kv_bytes / t_kv / 1e9,
                      "note": "latency-bound at this size (one 1152-byte row per warp)"},
@@ -438,6 +449,9 @@ def measure_next_rows(sfa, inp, peaks, flush):
         "topk": {"us": t_tk * 1e6, "shape": f"[{T},{S}] -> [{T},{w.top_k}]",
                  "roofline": {"bound": "hbm", "achieved": tk_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": tk_gbs / peaks["hbm_gbs"], "bytes": tk_bytes}},
+        "lse_merge": {"us": t_mg * 1e6, "shape": f"[{lw.n_splits},{lw.T},{lw.h},512] -> [{lw.T},{lw.h},512]",
+                      "roofline": {"bound": "hbm", "achieved": mg_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": mg_gbs / peaks["hbm_gbs"], "bytes": mg_bytes}},
     }
 
 
@@ -517,7 +531,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
-                    help="skip timing the kv_write / uv_proj / topk rows around the decode step")
+                    help="skip timing the kv_write / uv_proj / topk / lse_merge rows around the decode step")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's B (smaller cases for profiler captures)")
     args = ap.parse_args()
