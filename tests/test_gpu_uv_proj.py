@@ -28,3 +28,26 @@ def test_uv_proj_within_the_rounding_bound(T, h):
     err = np.abs(y.double().cpu().numpy() - ref)
     bound = 2.0 ** -8 * absprod + 2.0 ** -8 * np.abs(ref) + 1e-6
     assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3f}"
+
+
+def test_uv_proj_bounded_wait_timeout_is_reported_and_context_survives():
+    """A one-poll wait cap makes the W_UV kernel's waits give up: it reports
+    SFA_ERR_DEVICE_TIMEOUT (or finishes in time), drains its own loads, and the next
+    call computes the right result."""
+    g = torch.Generator().manual_seed(90)
+    out = (0.3 * torch.randn((64, 128, 512), generator=g)).float().cuda()
+    w = (torch.randn((128, 512, 128), generator=g) / 512 ** 0.5).to(torch.bfloat16).cuda()
+    sfa.last_device_status()
+    prev = sfa.set_wait_limit(1)
+    try:
+        sfa.uv_proj(out, w)
+        status = sfa.last_device_status()
+    finally:
+        sfa.set_wait_limit(prev)
+    assert status in (-5, 0)
+    y = sfa.uv_proj(out, w)
+    torch.cuda.synchronize()
+    assert sfa.last_device_status() == 0
+    ref = oracle.uv_proj(out.double().cpu().numpy(), w.cpu())
+    absprod = np.einsum("thc,hcv->thv", np.abs(out.double().cpu().numpy()), np.abs(w.double().cpu().numpy()))
+    assert np.all(np.abs(y.double().cpu().numpy() - ref) <= 2.0 ** -8 * absprod + 2.0 ** -8 * np.abs(ref) + 1e-6)
