@@ -78,6 +78,67 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
   }
 }
 
+// n <= 8 shards of 512-wide rows: a lane owns 16-byte columns lane + 32j (j < 4) of the
+// row.  All of its partial loads go out together with the lse loads, in two rounds of 16,
+// so the weights are computed while the rows are in flight instead of before.
+constexpr int kFastShards = 8;
+constexpr int kFastCols4 = 512 / 4 / 32;   // float4 columns per lane
+
+__global__ void __launch_bounds__(256) lse_merge_fast_kernel(const float* __restrict__ out_part,
+                                                             const float* __restrict__ lse_part, int n,
+                                                             int rows, float* __restrict__ out,
+                                                             float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int warps_per_block = blockDim.x >> 5;
+  const long long stride = (long long)gridDim.x * warps_per_block;
+  const size_t rstride4 = (size_t)rows * 512 / 4;   // float4s between shards
+  for (long long row = (long long)blockIdx.x * warps_per_block + (threadIdx.x >> 5); row < rows;
+       row += stride) {
+    const float lv = lane < n ? lse_part[(size_t)lane * rows + row] : -INFINITY;
+    const float4* base = reinterpret_cast<const float4*>(out_part + (size_t)row * 512) + lane;
+    float4 acc[kFastCols4];
+    float w = 0.f, L = -INFINITY;
+    bool empty = false;
+#pragma unroll
+    for (int j0 = 0; j0 < kFastCols4; j0 += 2) {
+      float4 v[2][kFastShards];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int u = 0; u < kFastShards; ++u)
+          v[jj][u] = u < n ? __ldg(base + (size_t)u * rstride4 + 32 * (j0 + jj)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j0 == 0) {   // the weights, while the first round of rows is in flight
+        const float M = warp_max(lv);
+        empty = M == -INFINITY;
+        if (!empty) {
+          const float Z = warp_sum(lane < n ? expf(lv - M) : 0.f);
+          L = M + logf(Z);
+          w = lane < n ? expf(lv - L) : 0.f;   // exactly 0 for an empty shard
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kFastShards; ++u) {
+          const float wu = __shfl_sync(0xffffffffu, w, u);
+          if (u < n && wu != 0.f) {
+            a.x += wu * v[jj][u].x;
+            a.y += wu * v[jj][u].y;
+            a.z += wu * v[jj][u].z;
+            a.w += wu * v[jj][u].w;
+          }
+        }
+        acc[j0 + jj] = a;
+      }
+    }
+    float4* orow = reinterpret_cast<float4*>(out + (size_t)row * 512) + lane;
+#pragma unroll
+    for (int j = 0; j < kFastCols4; ++j) orow[32 * j] = empty ? make_float4(0.f, 0.f, 0.f, 0.f) : acc[j];
+    if (lane == 0) lse[row] = empty ? -INFINITY : L;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,
@@ -91,7 +152,12 @@ cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n
   const long long cap = (long long)sms * 8;
   if (blocks > cap) blocks = cap;
   const bool vec4 = (dv % 4) == 0;
-  if (vec4)
+  const bool fast = dv == 512 && n_splits <= kFastShards && (reinterpret_cast<uintptr_t>(out_part) % 16) == 0 &&
+                    (reinterpret_cast<uintptr_t>(out) % 16) == 0;
+  if (fast)
+    lse_merge_fast_kernel<<<(int)blocks, warps_per_block * 32, 0, stream>>>(out_part, lse_part, n_splits, rows,
+                                                                            out, lse);
+  else if (vec4)
     lse_merge_kernel<true><<<(int)blocks, warps_per_block * 32, 0, stream>>>(
         out_part, lse_part, n_splits, rows, dv, out, lse);
   else
