@@ -76,6 +76,9 @@ PER_TOKEN = [
     W("bt_h128_q3", B=2, Q=3, h=128, S=2500, S_min=1, top_k=600, n_splits=1, index_kind="causal", seed=42),
     W("bt_h5_q4_bs16", B=2, Q=4, h=5, S=500, S_min=1, top_k=130, n_splits=1, index_kind="causal",
       block_size=16, seed=43),
+    # more than 2048 valid entries: the tensor-core kernel refills its resolved list
+    W("bt_h128_q2_k3000", B=1, Q=2, h=128, S=8192, S_min=4000, top_k=3000, n_splits=1, index_kind="causal",
+      seed=44),
 ]
 
 
