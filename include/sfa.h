@@ -9,7 +9,10 @@
  *  - Pointers marked "device" must point to memory of the current CUDA device;
  *    pointers marked "host" to host memory (pinned memory gives asynchronous
  *    copies).  The caller allocates and owns every buffer; the library never
- *    allocates, frees or keeps a pointer after a call returns.
+ *    allocates, frees or keeps a pointer after a call returns, with three stated
+ *    exceptions: an sfa_host_plan keeps the pointers it was created with,
+ *    sfa_decode_noalloc works in a fixed device array of the library's own, and
+ *    sfa_decode_host creates its helper streams and events once per device.
  *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
  *    default stream).  Calls only enqueue work on it and return without
  *    synchronising, except sfa_last_device_status() and the host-buffer entry
