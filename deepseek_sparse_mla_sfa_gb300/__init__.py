@@ -293,7 +293,7 @@ def kv_write(kv, slot_mapping, rows, stream=None):
     gets row slot_mapping[t] = rows[t] for every t with slot_mapping[t] >= 0, in place.
 
     kv [num_blocks, block_size, 576] bf16, slot_mapping [T] int32, rows [T, 576] bf16, all on
-    one CUDA device.  Returns kv.
+    one CUDA device.  A slot named twice ends up holding parts of both rows.  Returns kv.
     """
     lib = _lib.load()
     dev = kv.device

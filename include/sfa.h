@@ -193,8 +193,9 @@ sfa_status sfa_topk(const float *scores, long long row_stride, const int32_t *se
  *   slot_mapping  device int32 [T]: the slot of each new token; < 0 = padding (skipped)
  *   rows          device bf16 [T, 576]: the new latent rows
  *   T >= 0, num_slots >= 0; kv and rows 16-byte aligned.
- * Two tokens naming the same slot leave one of their rows there (which one is not
- * defined).  A slot >= num_slots writes nothing and sets SFA_ERR_DEVICE_BAD_BLOCK in
+ * Two tokens naming the same slot write it concurrently: the slot ends up holding parts
+ * of their rows, which parts is not defined (a slot mapping names each slot once).  A
+ * slot >= num_slots writes nothing and sets SFA_ERR_DEVICE_BAD_BLOCK in
  * the device status word.  Returns SFA_OK or a host-side argument error, nothing launched.
  */
 sfa_status sfa_kv_write(void *kv, long long num_slots, const int32_t *slot_mapping, const void *rows, int T,
