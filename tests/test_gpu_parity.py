@@ -40,6 +40,11 @@ SMALL = [
     W("h128_n64", B=2, Q=1, h=128, S=4096, top_k=700, n_splits=64, index_kind="uniform", seed=18),
     # a single selected position per token
     W("h128_k1", B=3, Q=1, h=128, S=1000, top_k=1, n_splits=1, index_kind="uniform", seed=19),
+    # a list eight times longer than the resolved segment (seven refills), with a ragged tail
+    W("h128_k16000", B=1, Q=1, h=128, S=20000, top_k=16000, n_splits=1, index_kind="uniform", seed=20),
+    # a large block: 1024 positions per block-table entry
+    W("h64_bs1024", B=2, Q=1, h=64, S=5000, top_k=1500, n_splits=2, index_kind="uniform", block_size=1024,
+      seed=22),
 ]
 
 
