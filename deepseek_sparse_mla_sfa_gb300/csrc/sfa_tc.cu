@@ -515,9 +515,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kProducerWarp + kProducerWarps) {
     // =================== gathers ===================================================
-    // Producer warp pw issues, from one lane, the gathers of row groups g = pw, pw+4,
-    // .. (4 rows each) of every tile: a single TMA-issuing lane per warp and several
-    // warps in parallel keep the gather engine busiest.
+    // Producer warp pw issues the gathers of row groups g = pw, pw+4, .. (4 rows each)
+    // of every tile, twenty per tile, one per lane in a single instruction: issue from
+    // several warps and several lanes keeps the gather engine busiest.
     const int pw = warp - kProducerWarp;
     int seg = 0;   // which kListCap-row segment of the resolved list is in list_s
     int n = 0;
@@ -541,24 +541,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      if (lane == 0) {
-        char* st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageTx / kProducerWarps);
-#pragma unroll 1
-        for (int g = pw; g < kNt / 4; g += kProducerWarps) {
-          int rr[4];
+      // one gather per lane: lane l takes column block l % 5 (four latent blocks, then
+      // the rope block) of the warp's row group l / 5, so the warp issues its twenty
+      // gathers of the tile as one instruction
+      char* st = smem + s * kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageTx / kProducerWarps);
+      __syncwarp();
+      constexpr int kGroupsPerWarp = kNt / 4 / kProducerWarps;
+      if (lane < 5 * kGroupsPerWarp) {
+        const int g = pw + kProducerWarps * (lane / 5), j = lane % 5;
+        int rr[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int e = first + 4 * g + k;
-            rr[k] = e < total ? list_s[e - seg * kListCap] : tp.num_rows;   // past the end: zero fill
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_gather4(smem_u32(st + j * kLatBlk + g * 4 * 128), &tmap_lat, 256 * crank + 64 * j, rr[0], rr[1], rr[2],
-                        rr[3], &bars[kBarKvFull + s]);
+        for (int k = 0; k < 4; ++k) {
+          const int e = first + 4 * g + k;
+          rr[k] = e < total ? list_s[e - seg * kListCap] : tp.num_rows;   // past the end: zero fill
+        }
+        if (j < 4)
+          tma_gather4(smem_u32(st + j * kLatBlk + g * 4 * 128), &tmap_lat, 256 * crank + 64 * j, rr[0], rr[1], rr[2],
+                      rr[3], &bars[kBarKvFull + s]);
+        else
           tma_gather4(smem_u32(st + 4 * kLatBlk + g * 4 * 64), &tmap_rope, 512 + 32 * crank, rr[0], rr[1], rr[2], rr[3],
                       &bars[kBarKvFull + s]);
-        }
       }
       __syncwarp();
     }
