@@ -47,3 +47,12 @@ def test_headline_workload_totals():
     assert abs(acc["flops"] / 1e9 - 36.51) < 0.01
     assert abs(acc["total_bytes"] / 1e6 - 177.8) < 0.1
     assert acc["merge_bytes"] == 0
+
+
+def test_committed_decode_traffic_matches_the_current_kernel_sources():
+    """The roofline's DRAM traffic comes from a committed ncu capture that names the hash
+    of the kernel sources it was taken from; a kernel or header change without a new
+    capture would leave the bench reporting no traffic for the headline kernel."""
+    assert bench.read_traffic("decode", True, "sfa_h128") is not None, (
+        "profiles/dram_traffic.txt has no entry for the current decode kernel sources: "
+        "recapture the decode profile")
