@@ -375,6 +375,12 @@ def run_ours(args, world, rank, local):
         "gather_gbs": gather_gbs, "algorithmic_gbs": alg_gbs,
         "pct_of_roofline": 100.0 * roof_s / (ms * 1e-3),
         "roofline_time_us": roof_s * 1e6,
+        # the step's tensor work against the measured bf16 peaks: the burst figure for a
+        # kernel timed alone, the seconds-long sustained figure beside it
+        "tensor": {"tflops": value / world,
+                   "frac_of_burst": value / world / peaks["bf16_tflops"],
+                   "frac_of_sustained": value / world / peaks["bf16_tflops_sustained"],
+                   "peak_burst": peaks["bf16_tflops"], "peak_sustained": peaks["bf16_tflops_sustained"]},
         "kernel_path": "tcgen05" if tc_path else "cuda-core",
         "kernels": {"decode_ms": dec_avg, "lse_merge_ms": mrg_avg if n > 1 else None},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved,
