@@ -26,8 +26,8 @@
 // shared-memory operand of the rope columns of QK^T.
 //
 // Warp roles (448 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
-// TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, one lane
-// each), warp 8 issues QK^T, warp 9 issues P.V, warps 10-13 send each tile's
+// TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, twenty
+// lanes each), warp 8 issues QK^T, warp 9 issues P.V, warps 10-13 send each tile's
 // partial scores to the peer as soon as QK^T has produced them (warp w serves TMEM
 // lane quadrant w % 4).  Every wait is bounded; a wait that gives up records
 // SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
@@ -50,7 +50,7 @@ constexpr int kStages = 4;       // gather pipeline depth
 constexpr int kHeads = 128;      // heads per unit (padded)
 constexpr int kThreads = 448;
 constexpr int kWarps = kThreads / 32;
-constexpr int kProducerWarp = 4;  // warps 4..7 issue the gathers (one lane each)
+constexpr int kProducerWarp = 4;  // warps 4..7 issue the gathers (twenty lanes each)
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = 8;        // issues QK^T
 constexpr int kPvWarp = 9;         // issues P.V
