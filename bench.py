@@ -362,6 +362,10 @@ def run_ours(args, world, rank, local):
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         cpu, _ = cpu_oracle_leg(inp, acc, target_s=15.0)
     next_rows = None if args.no_next_rows else measure_next_rows(sfa, inp, peaks, flush)
+    configs = None
+    if not args.no_configs and rank == 0:
+        mine = {"decode_us": dec_avg * 1e3, "merge_us": mrg_avg * 1e3 if n > 1 else None, "step_us": ms * 1e3}
+        configs = measure_configs(sfa, peaks, flush, w.name, mine, acc, steps=max(10, min(args.steps, 30)))
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -390,6 +394,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "gpu_launches": launches_per_step * args.steps,
         "next_rows": next_rows,
+        "configs": configs,
         "clocks": clk,
     }
     if rank == 0:
@@ -476,6 +481,87 @@ def measure_next_rows(sfa, inp, peaks, flush):
     }
 
 
+def roofline_of(acc, peaks):
+    """Roofline time of one step: the slower of the tensor work at the measured bf16 peak
+    and the algorithmic bytes at the measured HBM bandwidth."""
+    t_tensor = acc["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = acc["total_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    return max(t_tensor, t_hbm), ("tensor" if t_tensor > t_hbm else "hbm")
+
+
+def measure_configs(sfa, peaks, flush, measured_name, measured, measured_acc, steps=20):
+    """Every workload's step (decode, plus the lse merge when it is sharded) timed alone
+    with CUDA events on the launching stream, L2 scrubbed before each step, with its
+    algorithmic bytes and FLOPs (the same accounting as the headline) and its fraction of
+    the roofline.  The workload the headline step already timed is reported from that
+    measurement."""
+    res = {}
+    for name, w in workloads.CONFIGS.items():
+        if name not in ("tiny", "dense", "sfa_h128", "mtp", "long_dcp"):
+            continue
+        if name == measured_name:
+            acc, times = measured_acc, dict(measured)
+        else:
+            inp = workloads.make(w, device="cuda")
+            acc = accounting(inp)
+            n, T, h = w.n_splits, w.T, w.h
+            dev = inp.q.device
+            out = torch.empty((T, h, 512), dtype=torch.float32, device=dev)
+            lse = torch.empty((T, h), dtype=torch.float32, device=dev)
+            op = torch.empty((n, T, h, 512), dtype=torch.float32, device=dev) if n > 1 else None
+            lp = torch.empty((n, T, h), dtype=torch.float32, device=dev) if n > 1 else None
+
+            def step(evs=None):
+                if evs:
+                    evs[0].record()
+                if n > 1:
+                    sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                               n_splits=n, Q=w.Q, merge=False, out_part=op, lse_part=lp)
+                    if evs:
+                        evs[1].record()
+                    sfa.lse_merge(op, lp, out=out, lse=lse)
+                else:
+                    sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                               n_splits=1, Q=w.Q, out=out, lse=lse)
+                    if evs:
+                        evs[1].record()
+                if evs:
+                    evs[2].record()
+
+            for _ in range(3):
+                flush()
+                step()
+            torch.cuda.synchronize()
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+            for k in range(steps):
+                flush()
+                hold_device()
+                step(evs[k])
+            torch.cuda.synchronize()
+            if sfa.last_device_status() != 0:
+                raise RuntimeError(f"device status error in workload {name}")
+            dec = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+            mrg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+            times = {"decode_us": dec, "merge_us": mrg if n > 1 else None,
+                     "step_us": dec + (mrg if n > 1 else 0.0)}
+            del inp, out, lse, op, lp
+            torch.cuda.empty_cache()
+        step_s = times["step_us"] * 1e-6
+        roof_s, bound = roofline_of(acc, peaks)
+        entry = {"B": w.B, "Q": w.Q, "h": w.h, "S": w.S, "top_k": w.top_k, "n_splits": w.n_splits,
+                 **{k: v for k, v in times.items()},
+                 "flops": acc["flops"], "algorithmic_bytes": acc["total_bytes"],
+                 "gather_bytes": acc["gather_bytes"],
+                 "TFLOP/s": acc["flops"] / step_s / 1e12,
+                 "algorithmic_GB/s": acc["total_bytes"] / step_s / 1e9,
+                 "roofline_us": roof_s * 1e6, "bound": bound, "frac": roof_s / step_s}
+        if name == "tiny":
+            entry["bound"] = "latency"
+            entry["note"] = "a few KB of work: launch latency, not bandwidth, sets the time"
+        res[name] = entry
+    return res
+
+
 def read_traffic(kernel: str, tc_path: bool, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's sources (its
     .cu file, the host entry points and every header) still match the capture."""
@@ -542,6 +628,18 @@ def run_e2e(sfa, inp, steps, flush):
             "direct_call_ms_per_step": ms_direct}
 
 
+def spawn_ranks(n: int):
+    """Re-run this command as n replica ranks (one per GPU) under torch.distributed.run on
+    this node, rendezvous on 127.0.0.1; rank 0 prints the line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+    sys.exit(subprocess.call(cmd))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -553,6 +651,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip timing the kv_write / uv_proj / topk / lse_merge rows around the decode step")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the other workloads (the line's `configs` object)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's B (smaller cases for profiler captures)")
     args = ap.parse_args()
@@ -563,10 +663,17 @@ def main():
                                 name=f"{args.config}_b{args.batch}")
         workloads.CONFIGS[w.name] = w
         args.config = w.name
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and world_env == 1 and "LOCAL_RANK" not in os.environ:
+        # N replicas asked for without a launcher: start one rank per GPU through torchrun
+        spawn_ranks(args.gpus)
+        return
+    if world_env > 1 and args.gpus != world_env:
+        sys.exit(f"bench.py: --gpus {args.gpus} does not match WORLD_SIZE={world_env} of the launcher")
     if args.impl == "reference":
         # the reference arm is the CPU oracle: rank 0 alone runs it, the other ranks exit
         # without work, and no GPU or process group is needed
-        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        run_reference(args, world_env, int(os.environ.get("RANK", "0")))
         return
     world, rank, local = dist_setup()
     try:

@@ -25,7 +25,8 @@ MAX_SPLITS = 64
 BLOCK_TABLE_PER_TOKEN = 1   # sfa_decode_ex flag: one block-table row per query token
 
 __all__ = ["decode", "lse_merge", "decode_host", "decode_host_staging_bytes",
-           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path", "set_wait_limit", "kv_write", "uv_proj", "topk", "HostPlan",
+           "workspace_bytes", "decode_noalloc", "decode_launches", "last_device_status", "set_kernel_path",
+           "set_wait_limit", "set_stall_injection", "kv_write", "uv_proj", "topk", "HostPlan",
            "SfaError", "D_QK", "D_V", "BLOCK_TABLE_PER_TOKEN"]
 
 
@@ -52,6 +53,34 @@ def _need(t, name, dtype, device=None, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
 
 
+def _check_decode_inputs(q, kv, block_table, seq_lens, topk_idx, Q, block_table_per_token=False):
+    """The argument checks of every decode entry point: dtypes, ranks, the 576-column
+    rows and T == B*Q for q, the index lists and the block table (shapes first, so a bad
+    Q is reported even off the GPU), then one CUDA device for everything.  Returns
+    (T, h, B, top_k)."""
+    for t, name, dt, nd in ((q, "q", torch.bfloat16, 3), (kv, "kv", torch.bfloat16, 3),
+                            (block_table, "block_table", torch.int32, 2), (seq_lens, "seq_lens", torch.int32, 1),
+                            (topk_idx, "topk_idx", torch.int32, 2)):
+        _need(t, name, dt, None, nd)
+    T, h, d = q.shape
+    if d != D_QK or kv.shape[2] != D_QK:
+        raise ValueError("q and kv rows must have 576 columns")
+    if int(Q) != Q or Q < 1:
+        raise ValueError("Q must be an integer >= 1")
+    Q = int(Q)
+    B = seq_lens.shape[0]
+    bt_rows = T if block_table_per_token else B
+    if T != B * Q or topk_idx.shape[0] != T or block_table.shape[0] != bt_rows:
+        raise ValueError("inconsistent B / Q / T")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode runs on a CUDA device only")
+    for t, name in ((kv, "kv"), (block_table, "block_table"), (seq_lens, "seq_lens"), (topk_idx, "topk_idx")):
+        if t.device != dev:
+            raise ValueError(f"{name} must be on {dev}, got {t.device}")
+    return T, h, B, topk_idx.shape[1]
+
+
 def workspace_bytes(B: int, Q: int, h: int, top_k: int, n_splits: int) -> int:
     return int(_lib.load().sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits))
 
@@ -70,25 +99,11 @@ def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int =
     n_splits > 1 and merge=False returns the shard partials (out_part [n, B*Q, h, 512],
     lse_part [n, B*Q, h]).
     """
+    T, h, B, top_k = _check_decode_inputs(q, kv, block_table, seq_lens, topk_idx, Q, block_table_per_token)
     lib = _lib.load()
     dev = q.device
-    if dev.type != "cuda":
-        raise ValueError("decode runs on a CUDA device only")
-    _need(q, "q", torch.bfloat16, dev, 3)
-    _need(kv, "kv", torch.bfloat16, dev, 3)
-    _need(block_table, "block_table", torch.int32, dev, 2)
-    _need(seq_lens, "seq_lens", torch.int32, dev, 1)
-    _need(topk_idx, "topk_idx", torch.int32, dev, 2)
-    T, h, d = q.shape
-    if d != D_QK or kv.shape[2] != D_QK:
-        raise ValueError("q and kv rows must have 576 columns")
-    B = seq_lens.shape[0]
-    bt_rows = T if block_table_per_token else B
-    if T != B * Q or topk_idx.shape[0] != T or block_table.shape[0] != bt_rows:
-        raise ValueError("inconsistent B / Q / T")
     if interleave < 0:
         raise ValueError("interleave must be >= 0")
-    top_k = topk_idx.shape[1]
     num_blocks, block_size = kv.shape[0], kv.shape[1]
     max_blocks = block_table.shape[1]
     if n_splits == 1 or merge:
@@ -98,6 +113,8 @@ def decode(q, kv, block_table, seq_lens, topk_idx, scale: float, n_splits: int =
             lse = torch.empty((T, h), dtype=torch.float32, device=dev)
         _need(out, "out", torch.float32, dev)
         _need(lse, "lse", torch.float32, dev)
+        if tuple(out.shape) != (T, h, D_V) or tuple(lse.shape) != (T, h):
+            raise ValueError(f"out must be [{T}, {h}, {D_V}] and lse [{T}, {h}]")
     if n_splits > 1:
         if out_part is None:
             out_part = torch.empty((n_splits, T, h, D_V), dtype=torch.float32, device=dev)
@@ -133,21 +150,17 @@ def decode_noalloc(q, kv, block_table, seq_lens, topk_idx, scale: float, n_split
     Pass preallocated `out` [B*Q, h, 512] and `lse` [B*Q, h] fp32 to allocate nothing here.
     Calls that overlap on the GPU share that array and race.
     """
+    T, h, B, _ = _check_decode_inputs(q, kv, block_table, seq_lens, topk_idx, Q)
     lib = _lib.load()
     dev = q.device
-    _need(q, "q", torch.bfloat16, dev, 3)
-    _need(kv, "kv", torch.bfloat16, dev, 3)
-    _need(block_table, "block_table", torch.int32, dev, 2)
-    _need(seq_lens, "seq_lens", torch.int32, dev, 1)
-    _need(topk_idx, "topk_idx", torch.int32, dev, 2)
-    T, h, _ = q.shape
-    B = seq_lens.shape[0]
     if out is None:
         out = torch.empty((T, h, D_V), dtype=torch.float32, device=dev)
     if lse is None:
         lse = torch.empty((T, h), dtype=torch.float32, device=dev)
     _need(out, "out", torch.float32, dev)
     _need(lse, "lse", torch.float32, dev)
+    if tuple(out.shape) != (T, h, D_V) or tuple(lse.shape) != (T, h):
+        raise ValueError(f"out must be [{T}, {h}, {D_V}] and lse [{T}, {h}]")
     code = lib.sfa_decode_noalloc(_ptr(q), _ptr(kv), _ptr(block_table), _ptr(seq_lens),
                                   _ptr(topk_idx), B, Q, h, topk_idx.shape[1], kv.shape[0],
                                   kv.shape[1], block_table.shape[1], float(scale), n_splits,
@@ -370,6 +383,13 @@ def set_kernel_path(path: int) -> int:
     if prev < 0:
         raise ValueError("path must be 0 or 1")
     return prev
+
+
+def set_stall_injection(on: bool) -> bool:
+    """Test hook (C ABI ``sfa_set_stall_injection``): kernels with bounded waits launched
+    afterwards first wait on a barrier nothing completes, so their wait limit runs out and
+    they report SFA_ERR_DEVICE_TIMEOUT.  Returns the previous setting."""
+    return bool(_lib.load().sfa_set_stall_injection(1 if on else 0))
 
 
 def set_wait_limit(iterations: int) -> int:

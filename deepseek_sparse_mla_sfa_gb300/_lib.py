@@ -39,6 +39,7 @@ SIGNATURES = {
     "sfa_set_wait_limit": ([ctypes.c_longlong], ctypes.c_longlong),
     "sfa_decode_noalloc": ([P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, P, P], I),
     "sfa_set_kernel_path": ([I], I),
+    "sfa_set_stall_injection": ([I], I),
     "sfa_decode_launches": ([I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int)], I),
     "sfa_kv_write": ([P, ctypes.c_longlong, P, P, I, P], I),
     "sfa_topk": ([P, ctypes.c_longlong, P, I, I, I, I, P, P], I),

@@ -24,6 +24,7 @@ std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 std::atomic<long long> g_wait_limit{0};
 std::atomic<int> g_kernel_path{0};  // 0 automatic, 1 CUDA-core only
+std::atomic<int> g_stall{0};        // test hook: kernels first wait on a barrier nothing completes
 
 bool use_tc(int h, int block_size) { return g_kernel_path.load() == 0 && sfa::tc_supports(h, block_size); }
 constexpr long long kDefaultWaitLimit = 1LL << 26;  // iterations of a bounded device wait
@@ -120,6 +121,8 @@ int sfa_set_kernel_path(int path) {
 long long sfa_set_wait_limit(long long iterations) {
   return g_wait_limit.exchange(iterations < 0 ? 0 : iterations);
 }
+
+int sfa_set_stall_injection(int on) { return g_stall.exchange(on ? 1 : 0); }
 
 size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits) {
   if (B <= 0 || Q <= 0 || h <= 0 || top_k < 0 || n_splits < 1) return 0;
@@ -218,6 +221,7 @@ sfa_status sfa_decode_ex(const void* q, const void* kv, const int32_t* block_tab
   p.wait_limit = wl > 0 ? wl : kDefaultWaitLimit;
   p.interleave = interleave_size;
   p.bt_per_token = (flags & SFA_BLOCK_TABLE_PER_TOKEN) ? 1 : 0;
+  p.stall = g_stall.load();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool tc = use_tc(h, block_size) && sfa::tc_supports_ptrs(q, kv, p.out);
@@ -418,7 +422,7 @@ sfa_status sfa_uv_proj(const float* out, const void* w_uv, void* y, int T, int h
   int* status = status_word(dev);
   if (!status) return SFA_ERR_CUDA;
   const long long wl = g_wait_limit.load();
-  return sfa::launch_uv_proj(out, w_uv, y, T, h, wl > 0 ? wl : kDefaultWaitLimit, status,
+  return sfa::launch_uv_proj(out, w_uv, y, T, h, wl > 0 ? wl : kDefaultWaitLimit, g_stall.load(), status,
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SFA_OK
              : SFA_ERR_CUDA;

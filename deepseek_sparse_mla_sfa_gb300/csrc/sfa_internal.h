@@ -37,6 +37,7 @@ struct DecodeParams {
   long long wait_limit;   // iteration cap of every bounded device wait
   int interleave;         // > 0: shard r holds positions p with (p / interleave) % n_splits == r
   int bt_per_token;       // block_table has one row per query token (else one per sequence)
+  int stall;              // test hook: first wait on a barrier that nothing completes
 };
 
 // Record the first device-side error in the status word (never traps).
@@ -97,7 +98,7 @@ cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t prepare_decode_simt();
 cudaError_t prepare_decode_tc();
 cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, long long wait_limit,
-                           int* status, cudaStream_t stream);
+                           int stall, int* status, cudaStream_t stream);
 // Indexer top-k: cluster size C (CTAs per query token), positions per CTA and threads
 // per CTA for T tokens over S candidate positions on a GPU with n_sms SMs.
 void topk_plan(int T, int S, int n_sms, int& C, int& chunk, int& threads);

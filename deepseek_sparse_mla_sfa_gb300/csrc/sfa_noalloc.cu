@@ -11,7 +11,8 @@
 // The array is one per device, sized SFA_NOALLOC_SCRATCH_BYTES, and every GPU
 // that loads this library keeps it until the process exits.  Host code cannot
 // use the array's name as a device address, so its address is looked up once
-// per device (on the first call made with that device current) and cached.
+// per device (on the first call that needs scratch, with that device current) and
+// cached for the life of the process: a device reset invalidates it.
 // Every call overwrites all of the scratch it uses before reading it, so nothing
 // needs clearing between calls; calls that overlap on the GPU (two streams, or
 // two threads) share the one array and race.
@@ -49,6 +50,7 @@ extern "C" sfa_status sfa_decode_noalloc(const void* q, const void* kv, const in
                                          int Q, int h, int top_k, int num_blocks, int block_size,
                                          int max_blocks_per_seq, float scale, int n_splits,
                                          float* out, float* lse, sfa_stream stream) {
+  if (!out || !lse) return SFA_ERR_INVALID_ARG;   // no result buffer: nothing a caller could read
   if (B < 0 || Q < 1 || h < 1 || n_splits < 1 || top_k < 0) return SFA_ERR_INVALID_ARG;
   if (h > SFA_MAX_HEADS || n_splits > SFA_MAX_SPLITS) return SFA_ERR_UNSUPPORTED;
   const size_t T = (size_t)B * Q;
@@ -60,10 +62,14 @@ extern "C" sfa_status sfa_decode_noalloc(const void* q, const void* kv, const in
   if (need > (size_t)SFA_NOALLOC_SCRATCH_BYTES) return SFA_ERR_WORKSPACE;
   if (T == 0) return SFA_OK;
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
-  unsigned char* base = static_cast<unsigned char*>(scratch_address(dev));
-  if (!base) return SFA_ERR_CUDA;
+  // a call that needs no scratch does not touch the array (nor load or look it up)
+  unsigned char* base = nullptr;
+  if (need > 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;
+    base = static_cast<unsigned char*>(scratch_address(dev));
+    if (!base) return SFA_ERR_CUDA;
+  }
   float* out_part = n_splits > 1 ? reinterpret_cast<float*>(base) : nullptr;
   float* lse_part = n_splits > 1 ? reinterpret_cast<float*>(base + part_out) : nullptr;
   void* workspace = ws ? static_cast<void*>(base + part_out + part_lse) : nullptr;

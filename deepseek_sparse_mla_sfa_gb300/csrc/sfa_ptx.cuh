@@ -91,15 +91,17 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
   return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` polls or ~4 s, whichever first.  Returns
-// false when it gave up (the caller reports a timeout and unwinds).
+// Bounded wait: gives up after `limit` polls or `cap_ns` nanoseconds (4 s by default),
+// whichever first.  Returns false when it gave up (the caller reports a timeout and
+// unwinds).
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit,
+                                          uint64_t cap_ns = 4000000000ull) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (long long i = 1; i < limit; ++i) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 0 && globaltimer_ns() - t0 > 4000000000ull) return false;
+    if ((i & 255) == 0 && globaltimer_ns() - t0 > cap_ns) return false;
   }
   return false;
 }
@@ -245,14 +247,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-// same, arriving on the barrier at the same offset in every CTA of `mask`
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 // 32 lanes x 16 columns of 32 bits: thread i of the warp gets lane (base + i)

@@ -16,14 +16,15 @@
 //     probabilities, running max and sum agree bit for bit without exchanging them;
 //   * P.V is split by output columns: CTA c owns out[:, 256c : 256c+256), which
 //     are the latent columns it already holds (V is the latent part of the row).
-//     P (bf16) goes to a shared-memory tile, the A operand of P.V, so a score
-//     buffer is free for the next QK^T as soon as its scores have been read.
+//     P (bf16 pairs) overwrites the tile's partial scores in its TMEM score buffer
+//     and is the TMEM (A) operand of P.V; the buffer takes the next QK^T once
+//     P.V has read it.
 // Each CTA therefore reads 576 of the 1152 bytes of every selected row, once.
 // TMEM per CTA: O [128 heads x 256] fp32 (cols 0-255), q latent part (256-383,
-// bf16 pairs), two score buffers of 64 rows (384-511).  q arrives by TMA at kernel
-// start: its latent half lands in the (still idle) exchange and P buffers, from where
-// the softmax warps move it into TMEM, and its rope part lands in place as the
-// shared-memory operand of the rope columns of QK^T.
+// bf16 pairs), two score / probability buffers of 64 rows (384-511).  q arrives by
+// TMA at kernel start: its latent half lands in the (still idle) exchange buffers,
+// from where the softmax warps move it into TMEM, and its rope part lands in place
+// as the shared-memory operand of the rope columns of QK^T.
 //
 // Warp roles (448 threads): warps 0-3 softmax / rescale / epilogue (warp w owns
 // TMEM lanes 32w..32w+31 = heads 32w..32w+31), warps 4-7 gathers (TMA, twenty
@@ -31,6 +32,18 @@
 // partial scores to the peer as soon as QK^T has produced them (warp w serves TMEM
 // lane quadrant w % 4).  Every wait is bounded; a wait that gives up records
 // SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds without trapping.
+//
+// Ordering of the score exchange.  A sender copies its partials to the peer with
+// cp.async.bulk shared::cluster copies, which complete only on the peer's mbarrier
+// (mbarrier::complete_tx); the bulk async-group operations (commit_group /
+// wait_group.read) track only copies that complete through a bulk async-group, so
+// they say nothing about when such a copy has read its source.  Each 16-head slot
+// of the staging area is therefore written once per tile, and rewritten for tile j
+// only after the peer's softmax warps have arrived on our XFree barrier for tile j:
+// they do so after reading tile j-1 from their X buffer, which they do only once
+// every copy of tile j-1 has landed there, i.e. once every source slot has been read.
+// A softmax warp that gives up waiting still lets the copy of the tile it was
+// waiting for land (a time-capped drain) before the CTA exits.
 #include <atomic>
 #include <cuda.h>
 #include <string.h>
@@ -69,24 +82,25 @@ constexpr int kOffX = kOffQRope + kQRopeBytes;
 constexpr int kXBytes = kHeads * kNt * 4;               // partial scores [128 heads x 64 rows] fp32
 constexpr int kXWarpBytes = kXBytes / 4;                // the 32 heads of one warp
 constexpr int kXHalfBytes = kXWarpBytes / 2;            // 16 heads: one staging slot / bulk copy
-constexpr int kOffXStage = kOffX + kXBytes;             // outgoing partials, 16 heads per warp at once
-constexpr int kXStageBytes = 4 * kXHalfBytes;
-constexpr int kOffP = kOffXStage + kXStageBytes;        // P [128 heads x 64 rows] bf16, K-major SW128
-constexpr int kPBytes = kHeads * kNt * 2;
+// outgoing partials: one slot per 16 heads, so no slot is rewritten while a copy of the
+// same tile may still be reading it
+constexpr int kOffXStage = kOffX + kXBytes;
+constexpr int kXStageBytes = kXBytes;
 constexpr int kQBox = kHeads * 128;                     // one 64-column SW128 box of q's latent half
 constexpr int kOutBox = kHeads * 128;                   // one 32-column SW128 box of out (fp32)
 static_assert(8 * kOutBox <= kStages * kStageBytes, "out is staged in the gather stages");
-static_assert(4 * kQBox == kXBytes + kXStageBytes + kPBytes, "q's latent half fills X, staging and P");
-static_assert(kOffX % 1024 == 0 && kOffP % 1024 == 0, "SW128 operands need 1024-byte alignment");
-constexpr int kOffList = kOffP + kPBytes;
+static_assert(4 * kQBox == kXBytes + kXStageBytes, "q's latent half fills X and the staging slots");
+static_assert(kOffX % 1024 == 0, "SW128 boxes need 1024-byte alignment");
+constexpr int kOffList = kOffXStage + kXStageBytes;
 constexpr int kListCap = 2048;                          // resolved rows kept at once (multiple of kNt)
 constexpr int kOffBar = kOffList + kListCap * 4;
 // barriers
 constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQReady = kBarKvEmpty + kStages,
               kBarSFull = kBarQReady + 1, kBarSpFree = kBarSFull + 2, kBarOReady = kBarSpFree + 2,
-              kBarXFull = kBarOReady + 2, kBarXFree = kBarXFull + 1, kBarPvDone = kBarXFree + 1,
-              kBarPvFinal = kBarPvDone + 1, kBarMmaFin = kBarPvFinal + 1, kBarMmaFin2 = kBarMmaFin + 1,
-              kBarQLoad = kBarMmaFin2 + 1, kNumBars = kBarQLoad + 1;
+              kBarSFree = kBarOReady + 2, kBarXFull = kBarSFree + 2, kBarXFree = kBarXFull + 1,
+              kBarPvDone = kBarXFree + 1, kBarPvFinal = kBarPvDone + 1, kBarMmaFin = kBarPvFinal + 1,
+              kBarMmaFin2 = kBarMmaFin + 1, kBarQLoad = kBarMmaFin2 + 1, kBarNever = kBarQLoad + 1,
+              kNumBars = kBarNever + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 128 + 1024;        // + alignment slack
 static_assert(8 + 4 * kWarps <= 128, "misc area");
@@ -97,6 +111,7 @@ static_assert(kListCap % kNt == 0, "list segments hold whole tiles");
 // waits for this CTA's own copies / MMAs still in flight at exit use their own
 // (time-capped) limit, independent of the pipeline-wait cap
 constexpr long long kDrainLimit = 1LL << 40;
+constexpr uint64_t kDrainCapNs = 5000000ull;   // 5 ms: copies in flight land within microseconds
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384;
@@ -223,8 +238,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarQReady], 128);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kBarSFull + x], 1);     // QK^T of the tile in this score buffer done
-      mbar_init(&bars[kBarSpFree + x], 8);    // the 4 sender and 4 softmax warps read this buffer
-      mbar_init(&bars[kBarOReady + x], 128);  // probabilities in TMEM and O rescaled
+      mbar_init(&bars[kBarSpFree + x], 4);    // the 4 sender warps read this buffer's partials
+      mbar_init(&bars[kBarOReady + x], 128);  // probabilities in this buffer and O rescaled
+      mbar_init(&bars[kBarSFree + x], 1);     // P.V has read the probabilities: buffer free
     }
     mbar_init(&bars[kBarXFull], 1);           // arming arrival + the peer's 4 x 8 KB of partials
     mbar_init(&bars[kBarXFree], 4);           // the peer's 4 softmax warps read our partials (phase
@@ -234,6 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarMmaFin], 1);
     mbar_init(&bars[kBarMmaFin2], 1);
     mbar_init(&bars[kBarQLoad], 1);
+    mbar_init(&bars[kBarNever], 1);           // nothing arrives: the stall test hook waits on it
     *abort_s = 0;
     fence_barrier_init();
     // q of this token: latent columns [256c, 256c+256) as four SW128 boxes into the
@@ -366,21 +383,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     float m_ref = -INFINITY, l_sum = 0.f;  // running max (log2 units) and sum of this head
     if (warp == 0 && lane == 0 && n_tiles > 0) mbar_arrive_expect_tx(&bars[kBarXFull], x_bytes);
+    int x_seen = 0;   // tiles whose partials from the peer have landed in X
     for (int i = 0; i < n_tiles && !*abort_s; ++i) {
       const int bb = i & 1;
       // full scores of tile i = our partials (in this tile's TMEM score buffer) + the
-      // peer's (in X); both CTAs form the same fp32 sums.  Our partials are read first,
-      // which frees the score buffer for QK^T of tile i+2 without waiting for the peer.
+      // peer's (in X); both CTAs form the same fp32 sums.
       if (!wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       uint32_t v[4][16];
 #pragma unroll
       for (int c4 = 0; c4 < kNt / 16; ++c4) tmem_ld16(lane_base + kColS + kNt * bb + 16 * c4, v[c4]);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarSpFree + bb]);
       if (!wait_warp_cluster(&bars[kBarXFull], i & 1)) { fail(); break; }
+      x_seen = i + 1;
       if (warp == 0 && lane == 0 && i + 1 < n_tiles) mbar_arrive_expect_tx(&bars[kBarXFull], x_bytes);
       float s[kNt];
 #pragma unroll
@@ -437,17 +452,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < w2; ++j) sm[j] += sm[j + w2];
       l_sum = l_sum * alpha + sm[0];
-      // P.V of the previous tile has read the P tile (and O may be rescaled)
+      // probabilities (bf16 pairs) replace the partial scores in this tile's TMEM
+      // buffer once the sender warps have read them; P.V takes them from there
+      if (!wait_warp(&bars[kBarSpFree + bb], (i >> 1) & 1)) { fail(); break; }
+      tc_fence_after();
+      tmem_st16(lane_base + kColS + kNt * bb, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+      tmem_st16(lane_base + kColS + kNt * bb + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+      // O may be rescaled once P.V of the previous tile has completed
       if (i >= 1) {
         if (!wait_warp(&bars[kBarPvDone], (i - 1) & 1)) { fail(); break; }
         tc_fence_after();
       }
-      // probabilities (bf16 pairs): this head's row of the K-major SW128 P tile
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(smem + kOffP + head * 128 + ((c ^ (head & 7)) * 16)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
       // rescale this warp's O rows if any of its heads' reference max moved
       if (i >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
@@ -464,6 +479,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars[kBarOReady + bb]);
     }
+
+    // A softmax warp that gave up may leave the peer's copies of one more tile in
+    // flight into X (the peer sends tile j once we have read tile j-1): let them land,
+    // for at most a few milliseconds, before this CTA can exit.
+    if (*abort_s && warp == 0 && lane == 0 && x_seen < n_tiles)
+      (void)mbar_wait<true>(&bars[kBarXFull], x_seen & 1, kDrainLimit, kDrainCapNs);
 
     // ---- epilogue: out = O / l for this CTA's 256 columns; lse from CTA 0 --------
     // The normalised rows are staged in the (idle) gather stages as eight SW128 boxes
@@ -573,13 +594,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= kSendWarp) {
     // =================== partial-score senders =====================================
     // Sender warp w serves TMEM lane quadrant w % 4 (heads 32(w%4) .. +31): for every
-    // tile it loads our partial scores from the TMEM score buffer, stages them, and
-    // copies them into the peer's X buffer (one 8 KB bulk copy) as soon as QK^T is done.
+    // tile it loads our partial scores from the TMEM score buffer, stages them (lane l
+    // in the slot of heads 16(l/16) .. +15) and copies each slot holding real heads into
+    // the peer's X buffer as soon as QK^T is done.
     const int qd = warp & 3;
     const int head = qd * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-    char* xout = smem + kOffXStage + qd * kXHalfBytes + (lane & 15) * 256;   // this lane's staging row
-    char* xout_warp = smem + kOffXStage + qd * kXHalfBytes;
+    char* xout_warp = smem + kOffXStage + qd * kXWarpBytes;
+    char* xout = xout_warp + lane * 256;   // this lane's staging row
     const uint32_t xdst_warp = mapa(smem + kOffX + qd * kXWarpBytes, peer);
     const uint32_t xfull_peer = mapa(&bars[kBarXFull], peer);
     const int n_half = min(2, max(0, (p.h - 32 * qd + 15) / 16));   // this warp's 16-head slots with real heads
@@ -595,49 +617,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarSpFree + bj]);
+      if (lane == 0) mbar_arrive(&bars[kBarSpFree + bj]);   // the softmax may overwrite the buffer with P
       if (n_half == 0) continue;   // only padding heads in this quadrant
-      // the peer's X buffer holds its q (j = 0) or tile j-1 until all its warps have read it
+      // The peer has read tile j-1 from its X buffer (phase 0: moved its q out of it), so
+      // every copy of tile j-1 has landed there and has read its source slot.
       if (!(ok = wait_warp_cluster(&bars[kBarXFree], j & 1))) break;
-      // heads 0-15 of this warp, then heads 16-31, through one 4 KB staging slot
+      if ((lane >> 4) < n_half) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        if (hh >= n_half) break;
-        if (lane == 0 && (j >= 1 || hh == 1)) bulk_wait_read<0>();   // the slot's last copy has read it
-        __syncwarp();
-        if ((lane >> 4) == hh) {
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            *reinterpret_cast<uint4*>(xout + ((k ^ (head & 15)) * 16)) =
-                make_uint4(v[k >> 2][4 * (k & 3)], v[k >> 2][4 * (k & 3) + 1], v[k >> 2][4 * (k & 3) + 2],
-                           v[k >> 2][4 * (k & 3) + 3]);
-          fence_proxy_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) {
-          bulk_copy_s2cluster(xdst_warp + hh * kXHalfBytes, xout_warp, kXHalfBytes, xfull_peer);
-          bulk_commit_group();
-        }
+        for (int k = 0; k < 16; ++k)
+          *reinterpret_cast<uint4*>(xout + ((k ^ (head & 15)) * 16)) =
+              make_uint4(v[k >> 2][4 * (k & 3)], v[k >> 2][4 * (k & 3) + 1], v[k >> 2][4 * (k & 3) + 2],
+                         v[k >> 2][4 * (k & 3) + 3]);
+        fence_proxy_async_smem();
       }
+      __syncwarp();
+      if (lane == 0)
+        for (int hh = 0; hh < n_half; ++hh)
+          bulk_copy_s2cluster(xdst_warp + hh * kXHalfBytes, xout_warp + hh * kXHalfBytes, kXHalfBytes, xfull_peer);
       __syncwarp();
     }
     if (!ok) fail();
-    if (lane == 0) bulk_wait<0>();   // every copy this warp issued has landed
-    __syncwarp();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // =================== tcgen05 MMA issue: QK^T (warp 8) and P.V (warp 9) ========
     if (lane == 0 && n_tiles > 0) {
       bool ok = true;
       if (warp == kMmaWarp) {
-        ok = mbar_wait(&bars[kBarQReady], 0, wl);
+        // test hook: a wait that cannot complete, so the wait limit runs out
+        ok = !p.stall || mbar_wait(&bars[kBarNever], 0, wl);
+        ok = ok && mbar_wait(&bars[kBarQReady], 0, wl);
         tc_fence_after();
         const uint32_t id_qk = idesc_bf16(128, kNt, 0, 0);
         const uint32_t qrope_a = smem_u32(qrope);
         for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
           const int s = n % kStages, bb = n & 1;
           if (!(ok = mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl))) break;
-          // the score buffer is free once the senders and the softmax have read tile n-2
-          if (n >= 2 && !(ok = mbar_wait(&bars[kBarSpFree + bb], ((n >> 1) - 1) & 1, wl))) break;
+          // the score buffer is free once P.V has read tile n-2's probabilities from it
+          if (n >= 2 && !(ok = mbar_wait(&bars[kBarSFree + bb], ((n >> 1) - 1) & 1, wl))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * kStageBytes);
           const uint32_t d = tmem + kColS + kNt * bb;
@@ -653,17 +668,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         const uint32_t id_pv = idesc_bf16(128, 256, 0, 1);
-        const uint32_t p_tile = smem_u32(smem + kOffP);
         for (int n = 0; ok && n < n_tiles && !*abort_s; ++n) {
           const int s = n % kStages, bb = n & 1;
           if (!(ok = mbar_wait(&bars[kBarOReady + bb], (n >> 1) & 1, wl))) break;
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * kStageBytes);
+          // A = P [128 heads x 64 rows] bf16 pairs in TMEM, 16 rows (8 columns) per step
 #pragma unroll
           for (int k = 0; k < kNt / 16; ++k)
-            mma_ss(tmem + kColO, smem_desc(p_tile + 32 * k, 16, 1024, kSwizzle128),
+            mma_ts(tmem + kColO, tmem + kColS + kNt * bb + 8 * k,
                    smem_desc(st + 2048 * k, kLatBlk, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
           mma_commit(&bars[kBarKvEmpty + s]);
+          mma_commit(&bars[kBarSFree + bb]);
           mma_commit(&bars[kBarPvDone]);
           if (n == n_tiles - 1) mma_commit(&bars[kBarPvFinal]);
         }

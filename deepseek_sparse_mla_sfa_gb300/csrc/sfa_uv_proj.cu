@@ -33,7 +33,7 @@ constexpr int kWBlk = kC * 128;           // one 64-wide v block of W_UV[h]: 512
 constexpr int kWBytes = 2 * kWBlk;        // 128 KB
 constexpr int kOBlk = kTok * 128;         // one 64-column K block of the bf16 out tile
 constexpr int kOBytes = (kC / 64) * kOBlk;   // 64 KB
-constexpr int kSmemUV = kWBytes + kOBytes + 64 + 1024;
+constexpr int kSmemUV = kWBytes + kOBytes + 64 + 1024;   // + barriers and the TMEM address
 constexpr long long kDrainLimitUV = 1LL << 40;
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -43,19 +43,21 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kThreadsUV, 1)
     uv_proj_kernel(const __grid_constant__ CUtensorMap tmap_w, const float* __restrict__ out,
-                   __nv_bfloat16* __restrict__ y, int T, int h, long long wait_limit, int* status) {
+                   __nv_bfloat16* __restrict__ y, int T, int h, long long wait_limit, int stall, int* status) {
   extern __shared__ char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   char* w_s = smem;
   char* o_s = smem + kWBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWBytes + kOBytes);   // [0] W landed, [1] MMAs done
-  uint32_t* tmem_s = reinterpret_cast<uint32_t*>(bars + 2);
+  // [0] W landed, [1] MMAs done, [2] never completed (the stall test hook waits on it)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWBytes + kOBytes);
+  uint32_t* tmem_s = reinterpret_cast<uint32_t*>(bars + 3);
   const int head = blockIdx.y, t0 = blockIdx.x * kTok;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
     fence_barrier_init();
     // W_UV[h] as two 64-wide v blocks, each 512 rows of c (two 256-row boxes)
     mbar_arrive_expect_tx(&bars[0], kWBytes);
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(kThreadsUV, 1)
 
   bool issued = false;
   if (threadIdx.x == 0) {
-    if (mbar_wait(&bars[0], 0, wait_limit)) {
+    if ((!stall || mbar_wait(&bars[2], 0, wait_limit)) && mbar_wait(&bars[0], 0, wait_limit)) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(kVd, kTok, 1, 0);   // A MN-major (v contiguous), B K-major
       const uint32_t wa = smem_u32(w_s), ob = smem_u32(o_s);
@@ -171,7 +173,7 @@ EncodeTiledFnUV encode_fn_uv() {
 }  // namespace
 
 cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, int h, long long wait_limit,
-                           int* status, cudaStream_t stream) {
+                           int stall, int* status, cudaStream_t stream) {
   if (T == 0 || h == 0) return cudaSuccess;
   EncodeTiledFnUV fn = encode_fn_uv();
   if (!fn) return cudaErrorInvalidValue;
@@ -195,7 +197,7 @@ cudaError_t launch_uv_proj(const float* out, const void* w_uv, void* y, int T, i
   }
   const dim3 grid((unsigned)((T + kTok - 1) / kTok), (unsigned)h);
   uv_proj_kernel<<<grid, kThreadsUV, kSmemUV, stream>>>(wmap, out, static_cast<__nv_bfloat16*>(y), T, h, wait_limit,
-                                                        status);
+                                                        stall, status);
   return cudaGetLastError();
 }
 

@@ -93,9 +93,11 @@ typedef void *sfa_stream; /* a cudaStream_t */
  *               into them on the same stream (as sfa_lse_merge does).
  *   out_part, lse_part  device, fp32 [n_splits, B*Q, h, 512] and [n_splits, B*Q, h];
  *               required when n_splits > 1, ignored otherwise.
- *   workspace   device scratch of at least sfa_decode_workspace_bytes(...) bytes,
- *               256-byte aligned (may be NULL when that size is 0).  Its contents
- *               need no initialisation and are undefined afterwards.
+ *   workspace   reserved: device scratch of at least sfa_decode_workspace_bytes(...)
+ *               bytes, 256-byte aligned.  That size is 0 for every shape the current
+ *               kernels accept, so callers may pass NULL and 0; the argument keeps the
+ *               ABI stable for a kernel that needs scratch.  Contents need no
+ *               initialisation and are undefined afterwards.
  *   All float/bf16 buffers must be 16-byte aligned.
  * Returns SFA_OK, or an error code with nothing launched.
  */
@@ -107,8 +109,9 @@ sfa_status sfa_decode(const void *q, const void *kv, const int32_t *block_table,
                       sfa_stream stream);
 
 /*
- * sfa_decode_workspace_bytes -- device scratch sfa_decode needs for this shape
- * (internal split of long selections into chunks, merged on the device).  May be 0.
+ * sfa_decode_workspace_bytes -- device scratch sfa_decode needs for this shape.
+ * Reserved: 0 for every shape the current kernels accept (no kernel of this
+ * library uses scratch beyond its inputs and outputs).
  */
 size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits);
 
@@ -124,6 +127,8 @@ size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits);
  *
  *   out_part device fp32 [n_splits, rows, dv], lse_part device fp32 [n_splits, rows]
  *   out      device fp32 [rows, dv],           lse      device fp32 [rows]
+ *   (for decode partials rows = B*Q*h: the (token, head) pairs are merged alike, so
+ *   they are passed flattened rather than as separate token and head counts)
  *   1 <= n_splits <= 64, rows >= 0, dv >= 1; float buffers 16-byte aligned.
  *   out/lse must not overlap out_part/lse_part.
  */
@@ -309,6 +314,10 @@ sfa_status sfa_last_device_status(sfa_stream stream);
  *  - All calls share the one array: calls that overlap on the GPU (other streams,
  *    other threads) race.  Each call writes all the scratch it reads, so no
  *    clearing between calls is needed.
+ *  - A call with n_splits == 1 uses no scratch and does not look the array up.
+ *  - The looked-up address is cached per device for the life of the process; it is
+ *    not valid after a device reset (cudaDeviceReset), so no call may follow one.
+ *  - out or lse NULL returns SFA_ERR_INVALID_ARG before any other check.
  */
 #define SFA_NOALLOC_SCRATCH_BYTES (72u << 20)
 sfa_status sfa_decode_noalloc(const void *q, const void *kv, const int32_t *block_table,
@@ -344,6 +353,17 @@ const char *sfa_status_string(sfa_status s);
  * instead of hanging.  Returns the previous cap.
  */
 long long sfa_set_wait_limit(long long iterations);
+
+/*
+ * sfa_set_stall_injection -- test hook for the failure path: with on != 0, the
+ * kernels with bounded waits (the tcgen05 decode kernel and sfa_uv_proj) launched
+ * afterwards from this process first wait on a barrier that nothing ever completes.
+ * That wait runs out after the wait limit (sfa_set_wait_limit), the kernel records
+ * SFA_ERR_DEVICE_TIMEOUT, drains its own copies and matrix operations and returns:
+ * nothing faults, traps or hangs, and the context stays usable.  Returns the
+ * previous setting.
+ */
+int sfa_set_stall_injection(int on);
 
 #ifdef __cplusplus
 }

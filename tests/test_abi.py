@@ -83,6 +83,56 @@ def test_wait_limit_hook_roundtrip(lib):
     assert lib.sfa_set_wait_limit(old) == 123
 
 
+def test_stall_injection_hook_roundtrip(lib):
+    old = lib.sfa_set_stall_injection(5)           # any non-zero value turns it on
+    assert lib.sfa_set_stall_injection(old) == 1
+    assert lib.sfa_set_stall_injection(0) == old
+
+
+def test_workspace_is_reserved_and_zero(lib):
+    # no kernel of the library uses scratch: the reserved workspace size is 0 everywhere
+    for args in ((64, 1, 128, 2048, 1), (32, 1, 128, 2048, 8), (128, 2, 64, 2048, 1), (32, 1, 16, 8192, 4)):
+        assert lib.sfa_decode_workspace_bytes(*args) == 0
+
+
+def _noalloc(lib, out, lse, **kw):
+    a = dict(B=2, Q=1, h=4, top_k=8, nb=4, bs=64, mb=4, scale=0.07, n=2)
+    a.update(kw)
+    return lib.sfa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, a["B"], a["Q"], a["h"], a["top_k"], a["nb"],
+                                  a["bs"], a["mb"], a["scale"], a["n"], out, lse, P0)
+
+
+def test_noalloc_host_checks(lib):
+    # no result buffer: refused first, whatever else is wrong or empty
+    assert _noalloc(lib, P0, FAKE) == -1
+    assert _noalloc(lib, FAKE, P0) == -1
+    assert _noalloc(lib, P0, P0, B=0) == -1
+    assert _noalloc(lib, FAKE, FAKE, Q=0) == -1
+    assert _noalloc(lib, FAKE, FAKE, h=129) == -2
+    # partials beyond the fixed array: SFA_ERR_WORKSPACE, nothing launched
+    assert _noalloc(lib, FAKE, FAKE, B=144, h=128, n=2) == -3
+    assert _noalloc(lib, FAKE, FAKE, B=0, h=128, n=2) == 0   # empty batch within the limit
+
+
+def test_noalloc_binding_refuses_a_q_that_does_not_match_the_batch():
+    import torch
+
+    import deepseek_sparse_mla_sfa_gb300 as sfa
+    q = torch.zeros((4, 8, 576), dtype=torch.bfloat16)
+    kv = torch.zeros((4, 64, 576), dtype=torch.bfloat16)
+    bt = torch.zeros((2, 2), dtype=torch.int32)
+    sl = torch.full((2,), 64, dtype=torch.int32)
+    idx = torch.zeros((4, 16), dtype=torch.int32)
+    with pytest.raises(ValueError, match="B / Q / T"):     # T = 4 tokens are 2 sequences x Q=2
+        sfa.decode_noalloc(q, kv, bt, sl, idx, 0.07, n_splits=2, Q=1)
+    with pytest.raises(ValueError, match="B / Q / T"):
+        sfa.decode_noalloc(q, kv, bt, sl, idx, 0.07, n_splits=2, Q=3)
+    with pytest.raises(ValueError, match="576"):
+        sfa.decode_noalloc(q[:, :, :512].contiguous(), kv, bt, sl, idx, 0.07, Q=2)
+    with pytest.raises(ValueError, match="CUDA"):         # consistent shapes, but on the CPU
+        sfa.decode_noalloc(q, kv, bt, sl, idx, 0.07, n_splits=2, Q=2)
+
+
 def _decode_ex(lib, g, flags, **kw):
     a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, idx=FAKE, B=2, Q=1, h=4, top_k=8, nb=4, bs=64,
              mb=4, scale=0.07, n=2, out=FAKE, lse=FAKE, op=FAKE, lp=FAKE, ws=P0, wsb=0, stream=P0)

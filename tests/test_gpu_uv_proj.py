@@ -31,20 +31,22 @@ def test_uv_proj_within_the_rounding_bound(T, h):
 
 
 def test_uv_proj_bounded_wait_timeout_is_reported_and_context_survives():
-    """A one-poll wait cap makes the W_UV kernel's waits give up: it reports
-    SFA_ERR_DEVICE_TIMEOUT (or finishes in time), drains its own loads, and the next
-    call computes the right result."""
+    """The stall hook makes the W_UV kernel wait on a barrier that nothing completes: the
+    wait runs out under a short cap, the kernel reports SFA_ERR_DEVICE_TIMEOUT, drains its
+    own loads, and the next call computes the right result."""
     g = torch.Generator().manual_seed(90)
     out = (0.3 * torch.randn((64, 128, 512), generator=g)).float().cuda()
     w = (torch.randn((128, 512, 128), generator=g) / 512 ** 0.5).to(torch.bfloat16).cuda()
     sfa.last_device_status()
-    prev = sfa.set_wait_limit(1)
+    prev = sfa.set_wait_limit(1000)
+    prev_stall = sfa.set_stall_injection(True)
     try:
         sfa.uv_proj(out, w)
         status = sfa.last_device_status()
     finally:
+        sfa.set_stall_injection(prev_stall)
         sfa.set_wait_limit(prev)
-    assert status in (-5, 0)
+    assert status == -5
     y = sfa.uv_proj(out, w)
     torch.cuda.synchronize()
     assert sfa.last_device_status() == 0
