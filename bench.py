@@ -305,13 +305,13 @@ def run_ours(args, world, rank, local):
             if evs:
                 evs[1].record()
             sfa.lse_merge(op, lp, out=out, lse=lse)
+            if evs:
+                evs[2].record()
         else:
             sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
                        n_splits=1, Q=w.Q, out=out, lse=lse, workspace=ws)
             if evs:
                 evs[1].record()
-        if evs:
-            evs[2].record()
 
     for _ in range(args.warmup):
         flush()
@@ -336,7 +336,8 @@ def run_ours(args, world, rank, local):
     t_end = time.time()
     clk = clocks.stop(t_begin, t_end)
     dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    mrg_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    # a single-shard step is the decode launch alone (no merge event is recorded)
+    mrg_ms = [e[1].elapsed_time(e[2]) if n > 1 else 0.0 for e in evs]
     step_ms = [a + b for a, b in zip(dec_ms, mrg_ms)]
     local_ms = sum(step_ms) / max(1, len(step_ms))
     ms = max_over_ranks(local_ms, world)
@@ -385,7 +386,7 @@ def run_ours(args, world, rank, local):
                    "frac_of_burst": value / world / peaks["bf16_tflops"],
                    "frac_of_sustained": value / world / peaks["bf16_tflops_sustained"],
                    "peak_burst": peaks["bf16_tflops"], "peak_sustained": peaks["bf16_tflops_sustained"]},
-        "kernel_path": "tcgen05" if tc_path else "cuda-core",
+        "kernel_path": {2: "tcgen05 small-head", 1: "tcgen05 CTA pair", 0: "cuda-core"}[tc_path],
         "kernels": {"decode_ms": dec_avg, "lse_merge_ms": mrg_avg if n > 1 else None},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -481,6 +482,11 @@ def measure_next_rows(sfa, inp, peaks, flush):
     }
 
 
+# the headline shape with 16 heads: the small-head kernel's gather-bound case
+SMALL_HEAD = workloads.Workload("sfa_h16", B=64, Q=1, h=16, S=32768, top_k=2048, n_splits=1,
+                                index_kind="uniform", seed=1234 + 6)
+
+
 def roofline_of(acc, peaks):
     """Roofline time of one step: the slower of the tensor work at the measured bf16 peak
     and the algorithmic bytes at the measured HBM bandwidth."""
@@ -496,9 +502,9 @@ def measure_configs(sfa, peaks, flush, measured_name, measured, measured_acc, st
     the roofline.  The workload the headline step already timed is reported from that
     measurement."""
     res = {}
-    for name, w in workloads.CONFIGS.items():
-        if name not in ("tiny", "dense", "sfa_h128", "mtp", "long_dcp"):
-            continue
+    todo = [(n, w) for n, w in workloads.CONFIGS.items() if n in ("tiny", "dense", "sfa_h128", "mtp", "long_dcp")]
+    todo.append(("sfa_h16", SMALL_HEAD))
+    for name, w in todo:
         if name == measured_name:
             acc, times = measured_acc, dict(measured)
         else:
@@ -520,13 +526,13 @@ def measure_configs(sfa, peaks, flush, measured_name, measured, measured_acc, st
                     if evs:
                         evs[1].record()
                     sfa.lse_merge(op, lp, out=out, lse=lse)
+                    if evs:
+                        evs[2].record()
                 else:
                     sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
                                n_splits=1, Q=w.Q, out=out, lse=lse)
                     if evs:
                         evs[1].record()
-                if evs:
-                    evs[2].record()
 
             for _ in range(3):
                 flush()
@@ -541,7 +547,7 @@ def measure_configs(sfa, peaks, flush, measured_name, measured, measured_acc, st
             if sfa.last_device_status() != 0:
                 raise RuntimeError(f"device status error in workload {name}")
             dec = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
-            mrg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+            mrg = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3 if n > 1 else 0.0
             times = {"decode_us": dec, "merge_us": mrg if n > 1 else None,
                      "step_us": dec + (mrg if n > 1 else 0.0)}
             del inp, out, lse, op, lp
@@ -558,18 +564,24 @@ def measure_configs(sfa, peaks, flush, measured_name, measured, measured_acc, st
         if name == "tiny":
             entry["bound"] = "latency"
             entry["note"] = "a few KB of work: launch latency, not bandwidth, sets the time"
+        if name == "sfa_h16":
+            entry["note"] = ("not one of the five workloads: the headline shape with 16 heads, "
+                             "where the step is a gather with little arithmetic per byte")
+        entry["kernel"] = {2: "tcgen05 small-head", 1: "tcgen05 CTA pair", 0: "cuda-core"}[
+            sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1]]
         res[name] = entry
     return res
 
 
-def read_traffic(kernel: str, tc_path: bool, workload: str):
+def read_traffic(kernel: str, tc_path: int, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's sources (its
     .cu file, the host entry points and every header) still match the capture."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     from deepseek_sparse_mla_sfa_gb300 import build as _b
-    src = {"decode": "sfa_tc.cu" if tc_path else "sfa_simt.cu", "lse_merge": "sfa_merge.cu"}.get(kernel)
+    src = {"decode": {2: "sfa_narrow.cu", 1: "sfa_tc.cu", 0: "sfa_simt.cu"}[int(tc_path)],
+           "lse_merge": "sfa_merge.cu"}.get(kernel)
     if src is None:
         return None
     src_hash = _b.source_hash([src, "sfa_api.cu"])

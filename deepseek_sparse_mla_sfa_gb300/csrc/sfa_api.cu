@@ -23,10 +23,15 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_status_ptr[kMaxDevices] = {};
 std::atomic<long long> g_wait_limit{0};
-std::atomic<int> g_kernel_path{0};  // 0 automatic, 1 CUDA-core only
+std::atomic<int> g_kernel_path{0};  // 0 automatic, 1 CUDA-core only, 2 CTA-pair tcgen05 for every h
 std::atomic<int> g_stall{0};        // test hook: kernels first wait on a barrier nothing completes
 
-bool use_tc(int h, int block_size) { return g_kernel_path.load() == 0 && sfa::tc_supports(h, block_size); }
+// 0: CUDA-core kernel, 1: CTA-pair tcgen05 kernel, 2: small-head tcgen05 kernel
+int kernel_choice(int h, int block_size) {
+  const int path = g_kernel_path.load();
+  if (path == 1 || !sfa::tc_supports(h, block_size)) return 0;
+  return path == 0 && sfa::narrow_supports(h) ? 2 : 1;
+}
 constexpr long long kDefaultWaitLimit = 1LL << 26;  // iterations of a bounded device wait
 
 // helper streams of sfa_decode_host, created once per device on first use
@@ -114,7 +119,7 @@ const char* sfa_status_string(sfa_status s) {
 }
 
 int sfa_set_kernel_path(int path) {
-  if (path != 0 && path != 1) return -1;
+  if (path < 0 || path > 2) return -1;
   return g_kernel_path.exchange(path);
 }
 
@@ -135,8 +140,9 @@ int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_sp
   if (B < 0 || Q < 1 || h < 1 || h > SFA_MAX_HEADS || top_k < 0 || block_size < 1 ||
       n_splits < 1 || n_splits > SFA_MAX_SPLITS)
     return -1;
-  const bool tc = use_tc(h, block_size);
-  if (tensor_core_path) *tensor_core_path = tc ? 1 : 0;
+  const int choice = kernel_choice(h, block_size);
+  const bool tc = choice != 0;
+  if (tensor_core_path) *tensor_core_path = choice;
   if ((long long)B * Q == 0) return 0;
   int n = tc ? sfa::tc_launches(B * Q, h, top_k, n_splits) : 1;
   if (n_splits > 1 && merge) n += 1;
@@ -224,8 +230,9 @@ sfa_status sfa_decode_ex(const void* q, const void* kv, const int32_t* block_tab
   p.stall = g_stall.load();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool tc = use_tc(h, block_size) && sfa::tc_supports_ptrs(q, kv, p.out);
-  cudaError_t e = tc ? sfa::launch_decode_tc(p, s) : sfa::launch_decode_simt(p, s);
+  const int choice = kernel_choice(h, block_size);
+  const bool tc = choice != 0 && sfa::tc_supports_ptrs(q, kv, p.out);
+  cudaError_t e = tc ? sfa::launch_decode_tc(p, choice == 2, s) : sfa::launch_decode_simt(p, s);
   if (e != cudaSuccess) return SFA_ERR_CUDA;
   if (merge_after) {
     e = sfa::launch_lse_merge(out_part, lse_part, n_splits, T * h, SFA_D_V, out, lse, s);
@@ -375,7 +382,9 @@ sfa_status sfa_host_plan_create(const void* q_host, const void* kv, const int32_
   // everything that is set up once per device happens here, outside the capture
   if (!status_word(dev)) return SFA_ERR_CUDA;
   host_pipe(dev);
-  if (sfa::prepare_decode_tc() != cudaSuccess || sfa::prepare_decode_simt() != cudaSuccess) return SFA_ERR_CUDA;
+  if (sfa::prepare_decode_tc() != cudaSuccess || sfa::prepare_decode_narrow() != cudaSuccess ||
+      sfa::prepare_decode_simt() != cudaSuccess)
+    return SFA_ERR_CUDA;
   cudaStream_t cs = nullptr;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return SFA_ERR_CUDA;
   if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {

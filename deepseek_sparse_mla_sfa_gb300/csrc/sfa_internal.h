@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/sfa.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -109,12 +110,21 @@ cudaError_t launch_kv_write(void* kv, long long num_slots, const int32_t* slot_m
 cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,
                              int dv, float* out, float* lse, cudaStream_t stream);
 
-// tcgen05 path: whether it handles this problem, its workspace, and its launch.
+// tcgen05 path: whether it handles this problem, its workspace, and its launch.  Two
+// kernels: the CTA-pair kernel (any h <= 128) and the small-head kernel (h <= 32).
 bool tc_supports(int h, int block_size);
 // the tcgen05 path also needs 16-byte aligned q, kv and out (TMA tensor maps)
 bool tc_supports_ptrs(const void* q, const void* kv, const void* out);
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits);
 int tc_launches(int T, int h, int top_k, int n_splits);
-cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, bool small_heads, cudaStream_t stream);
+// the small-head kernel (sfa_narrow.cu): heads it serves, its one-time set-up, its
+// cluster size for `units` (token, shard) units on n_sms SMs, and its launch with the
+// cache-row map (64 columns x 1 row, 128-byte swizzle) and q's rope map (64 columns x h)
+bool narrow_supports(int h);
+cudaError_t prepare_decode_narrow();
+int narrow_cluster_size(long long units, int n_sms);
+cudaError_t launch_decode_narrow(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
+                                 cudaStream_t stream);
 
 }  // namespace sfa

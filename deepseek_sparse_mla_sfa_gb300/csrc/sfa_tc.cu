@@ -52,6 +52,7 @@
 
 #include "sfa_internal.h"
 #include "sfa_ptx.cuh"
+#include "sfa_resolve.cuh"
 
 namespace sfa {
 namespace {
@@ -122,77 +123,6 @@ struct TcParams {
   int num_rows;  // num_blocks * block_size (== out-of-range row used for padding)
   int q_rows;    // heads per q box: min(h, 128)
 };
-
-__device__ __forceinline__ int lanemask_lt() {
-  int m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-// 2^x on the special-function unit (inputs <= 8 here; -inf gives 0)
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// Physical cache row of selected entry `pos`, or -1 when the entry is padding for
-// this shard (or its block-table entry is invalid, which is reported).
-template <bool kInterleaved>
-__device__ __forceinline__ int resolve_row(const DecodeParams& p, int bt_row, int pos, const ShardSel& sel,
-                                           bool report) {
-  if (!sel.has_fixed<kInterleaved>(pos)) return -1;
-  const int blk = pos / p.block_size;
-  const int phys = blk < p.max_blocks ? p.block_table[(size_t)bt_row * p.max_blocks + blk] : -1;
-  if (phys < 0 || phys >= p.num_blocks) {
-    if (report) report_status(p.status, kStatusBadBlock);
-    return -1;
-  }
-  return phys * p.block_size + pos % p.block_size;
-}
-
-// One lane's share of a warp's chunk [c_begin, c_end) of the selected list, 8 entries
-// per lane per round: counts the entries that resolve to a cache row of this unit and
-// leaves the last round's rows in row_r (-1 for entries that do not).  The layout of the
-// shards is a template argument so that the loop carries no per-entry branch on it.
-template <bool kInterleaved>
-__device__ __forceinline__ int resolve_chunk(const DecodeParams& p, const int32_t* idx, int c_begin, int c_end,
-                                             int lane, const ShardSel& sel, int bt_row, bool report,
-                                             int (&row_r)[8]) {
-  int cnt = 0;
-  for (int j0 = c_begin; j0 < c_end; j0 += 32 * 8) {
-    int pos[8], blkv[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int j = j0 + 32 * k + lane;
-      pos[k] = j < c_end ? __ldg(idx + j) : -1;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const bool in = sel.has_fixed<kInterleaved>(pos[k]);
-      const int blk = in ? pos[k] / p.block_size : 0;
-      blkv[k] = in && blk < p.max_blocks ? __ldg(p.block_table + (size_t)bt_row * p.max_blocks + blk) : -2;
-      if (!in) blkv[k] = -3;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      row_r[k] = -1;
-      if (blkv[k] == -3) continue;
-      if (blkv[k] < 0 || blkv[k] >= p.num_blocks) {
-        if (report) report_status(p.status, kStatusBadBlock);
-      } else {
-        ++cnt;
-        row_r[k] = blkv[k] * p.block_size + pos[k] % p.block_size;
-      }
-    }
-  }
-  return cnt;
-}
 
 // kInterleaved: the shards are interleaved (interleave size > 0 and more than one shard);
 // the layout is fixed per instantiation so that no selection test branches on it.
@@ -346,7 +276,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // its slice, and the peer may write into ours once all four warps have arrived
     {
       bool qok = wait_warp(&bars[kBarQLoad], 0);
-      if (!qok) fail();
+      if (!qok) {
+        fail();
+        // the q load must land before this CTA can exit
+        if (warp == 0 && lane == 0 && !mbar_wait(&bars[kBarQLoad], 0, kDrainLimit))
+          report_status(p.status, kStatusTimeout);
+        __syncwarp();
+      }
       const bool have = qok && head < tp.q_rows;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -826,12 +762,20 @@ cudaError_t prepare_decode_tc() {
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_tc(const DecodeParams& p, bool small_heads, cudaStream_t stream) {
   const long long T = (long long)p.B * p.Q;
   const long long units = T * p.n_splits;
   if (units == 0) return cudaSuccess;
   const long long num_rows = (long long)p.num_blocks * p.block_size;
   if (num_rows >= 0x7fffffffLL || 2 * units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (small_heads) {
+    // whole rows as nine 64-column SW128 boxes from one map; q's rope columns as one box
+    CUtensorMap rows, qrope;
+    if (!narrow_supports(p.h) || !make_row_map(&rows, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_q_map(&qrope, p.q, p.h, T, p.h, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    return launch_decode_narrow(p, rows, qrope, stream);
+  }
   TcParams tp;
   tp.p = p;
   tp.num_rows = (int)num_rows;

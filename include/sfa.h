@@ -328,17 +328,20 @@ sfa_status sfa_decode_noalloc(const void *q, const void *kv, const int32_t *bloc
 /*
  * sfa_decode_launches -- how many kernels one sfa_decode call with these
  * arguments enqueues (merge != 0: out/lse given with n_splits > 1), and through
- * *tensor_core_path whether the tcgen05 kernel serves it (1) or the CUDA-core
- * kernel (0).  tensor_core_path may be NULL.  Returns -1 for invalid arguments.
+ * *tensor_core_path which kernel serves it: 2 = the small-head tcgen05 kernel
+ * (h <= 32), 1 = the CTA-pair tcgen05 kernel, 0 = the CUDA-core kernel.
+ * tensor_core_path may be NULL.  Returns -1 for invalid arguments.
  */
 int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_splits, int merge,
                         int *tensor_core_path);
 
 /*
  * sfa_set_kernel_path -- kernel family for sfa_decode calls made afterwards in
- * this process: 0 = automatic (the tcgen05 kernel wherever it applies), 1 = the
- * CUDA-core kernel for every shape (to cross-check the two).  Returns the
- * previous setting, or -1 (and changes nothing) for another value.
+ * this process: 0 = automatic (the small-head tcgen05 kernel for h <= 32, the
+ * CTA-pair tcgen05 kernel above), 1 = the CUDA-core kernel for every shape, 2 = the
+ * CTA-pair tcgen05 kernel for every shape.  Paths 1 and 2 exist to cross-check the
+ * kernels against each other.  Returns the previous setting, or -1 (and changes
+ * nothing) for another value.
  */
 int sfa_set_kernel_path(int path);
 

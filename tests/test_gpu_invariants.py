@@ -1,4 +1,4 @@
-"""Invariants of the CUDA path that hold at any size (both kernel paths):
+"""Invariants of the CUDA path that hold at any size (every kernel):
 
 * permuting the physical cache blocks, with a block table that follows, reads the same
   rows in the same order: bit-identical output;
@@ -19,13 +19,19 @@ from tests.gpu_helpers import compare, problem_of
 pytestmark = pytest.mark.gpu
 
 W = workloads.Workload
-CASE = W("inv", B=3, Q=2, h=128, S=5000, S_min=300, top_k=700, n_splits=1, index_kind="causal", seed=51)
+CASE_WIDE = W("inv", B=3, Q=2, h=128, S=5000, S_min=300, top_k=700, n_splits=1, index_kind="causal", seed=51)
+CASE_NARROW = W("inv_h16", B=3, Q=2, h=16, S=5000, S_min=300, top_k=700, n_splits=1, index_kind="causal", seed=52)
 
 
-@pytest.fixture(params=[0, 1], ids=["tcgen05", "cudacore"])
+# (kernel path, case): the tcgen05 kernels (automatic: CTA pair at h=128, small-head at
+# h=16; forced CTA pair at h=16) and the CUDA-core kernel
+@pytest.fixture(params=[(0, CASE_WIDE), (1, CASE_WIDE), (0, CASE_NARROW), (2, CASE_NARROW), (1, CASE_NARROW)],
+                ids=["pair-h128", "cudacore-h128", "small-h16", "pair-h16", "cudacore-h16"])
 def kernel_path(request):
-    prev = sfa.set_kernel_path(request.param)
-    yield request.param
+    global CASE
+    path, CASE = request.param
+    prev = sfa.set_kernel_path(path)
+    yield path
     sfa.set_kernel_path(prev)
 
 

@@ -39,11 +39,18 @@ INTERLEAVED = [
 CASES = [(w, g) for w, gs in INTERLEAVED for g in gs]
 
 
-@pytest.fixture(params=[0, 1], ids=["tcgen05", "cudacore"])
+# 0 automatic (small-head kernel for h <= 32, CTA pair above), 1 CUDA-core, 2 CTA pair for
+# every h (run only where it differs from the automatic choice)
+@pytest.fixture(params=[0, 1, 2], ids=["auto", "cudacore", "pair"])
 def kernel_path(request):
     prev = sfa.set_kernel_path(request.param)
     yield request.param
     sfa.set_kernel_path(prev)
+
+
+def _skip_duplicate(path, h):
+    if path == 2 and h > 32:
+        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 32")
 
 
 def _run(inp, bt, n, g, per_token, merge):
@@ -57,6 +64,7 @@ def _problem(inp, bt):
 
 @pytest.mark.parametrize("w,g", CASES, ids=[f"{w.name}-g{g}" for w, g in CASES])
 def test_interleaved_shards_every_element(w, g, kernel_path):
+    _skip_duplicate(kernel_path, w.h)
     inp = workloads.make(w, device="cuda")
     prob = problem_of(inp)
     op, lp = _run(inp, inp.block_table, w.n_splits, g, False, merge=False)
@@ -84,6 +92,7 @@ PER_TOKEN = [
 
 @pytest.mark.parametrize("w", PER_TOKEN, ids=[w.name for w in PER_TOKEN])
 def test_block_table_per_token_every_element(w, kernel_path):
+    _skip_duplicate(kernel_path, w.h)
     inp = workloads.make(w, device="cuda")
     bt = workloads.per_token_block_table(inp, shuffle=True, seed=w.seed)
     prob = _problem(inp, bt)
@@ -124,10 +133,11 @@ def test_interleave_size_one_shard_is_the_unsplit_kernel(kernel_path):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_long_dcp_interleaved_full_size_sampled():
+def test_long_dcp_interleaved_full_size_every_element():
     """The 8-shard long-context workload at full size with 64-position interleaving (one
-    launch over all shards plus the merge): sampled merged outputs against the unsplit
-    oracle, and sampled shard partials against the oracle's interleaved shards."""
+    launch over all shards plus the merge): every merged output against the unsplit
+    oracle, and every shard partial against the oracle's interleaved shards (shard r holds
+    the positions with (p / 64) % 8 == r)."""
     w = workloads.CONFIGS["long_dcp"]
     inp = workloads.make(w, device="cuda")
     op, lp = _run(inp, inp.block_table, w.n_splits, 64, False, merge=False)
@@ -135,13 +145,7 @@ def test_long_dcp_interleaved_full_size_sampled():
     torch.cuda.synchronize()
     assert sfa.last_device_status() == 0
     prob = problem_of(inp)
-    tt, hh = sample_pairs(w.T, w.h, 12, seed=5)
-    ref_out, ref_lse = oracle.decode_sampled(prob, tt, hh)
-    compare(out[tt, hh].double().cpu().numpy(), lse[tt, hh].double().cpu().numpy(), ref_out, ref_lse,
-            "long_dcp interleaved merged (sampled)")
-    # shard partials of sampled (shard, token, head) triples: shard r holds the positions
-    # with (p / 64) % 8 == r
-    rr = np.random.default_rng(6).integers(0, w.n_splits, tt.shape[0]).astype(np.int32)
-    rop, rlp = oracle.decode_sampled(prob, tt, hh, shards=rr, n_splits=w.n_splits, interleave=64)
-    compare(op[rr, tt, hh].double().cpu().numpy(), lp[rr, tt, hh].double().cpu().numpy(), rop, rlp,
-            "long_dcp interleaved shard partials (sampled)")
+    ref_out, ref_lse = oracle.decode(prob)
+    compare(out, lse, ref_out, ref_lse, "long_dcp interleaved merged")
+    rop, rlp = oracle.decode_ex(prob, w.n_splits, interleave=64)
+    compare(op, lp, rop, rlp, "long_dcp interleaved shard partials")

@@ -44,10 +44,23 @@ SMALL = [
     # a large block: 1024 positions per block-table entry
     W("h64_bs1024", B=2, Q=1, h=64, S=5000, top_k=1500, n_splits=2, index_kind="uniform", block_size=1024,
       seed=22),
+    # small-head kernel: clusters of 4 (few units), 2 and 1 CTAs per unit, both padded head
+    # counts (16, 32), CTAs of a cluster with no tile, a list longer than it keeps resolved
+    W("h32_g4", B=3, Q=1, h=32, S=3000, top_k=700, n_splits=1, index_kind="uniform", seed=40),
+    W("h16_g2", B=64, Q=1, h=16, S=8192, top_k=2048, n_splits=1, index_kind="uniform", seed=41),
+    W("h17_k3000_refill", B=1, Q=1, h=17, S=4096, top_k=3000, n_splits=1, index_kind="uniform", seed=42),
+    W("h8_one_tile", B=2, Q=1, h=8, S=500, top_k=40, n_splits=1, index_kind="uniform", seed=43),
+    W("h12_mtp_splits", B=5, Q=2, h=12, S=2500, S_min=30, top_k=400, n_splits=3, index_kind="causal", seed=44),
+    W("h2_bs16_g1", B=40, Q=1, h=2, S=900, top_k=300, n_splits=2, index_kind="uniform", block_size=16, seed=45),
 ]
 
+# which kernel decode_launches reports per kernel-path setting (0 automatic, 1 CUDA-core,
+# 2 CTA-pair tcgen05): 2 = small-head tcgen05, 1 = CTA-pair tcgen05, 0 = CUDA-core
+def expected_kernel(path, h):
+    return {1: 0, 2: 1}.get(path, 2 if h <= 32 else 1)
 
-@pytest.fixture(params=[0, 1], ids=["tcgen05", "cudacore"])
+
+@pytest.fixture(params=[0, 1, 2], ids=["auto", "cudacore", "pair"])
 def kernel_path(request):
     prev = sfa.set_kernel_path(request.param)
     yield request.param
@@ -56,7 +69,9 @@ def kernel_path(request):
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
 def test_small_cases_every_element(w, kernel_path):
-    assert sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1] == (kernel_path == 0)
+    if kernel_path == 2 and w.h > 32:
+        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 32")
+    assert sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1] == expected_kernel(kernel_path, w.h)
     inp = workloads.make(w, device="cuda")
     prob = problem_of(inp)
     ref_out, ref_lse = oracle.decode(prob)
@@ -74,6 +89,8 @@ def test_small_cases_every_element(w, kernel_path):
 
 
 FULL = ["tiny", "dense", "sfa_h128", "mtp", "long_dcp"]
+# the headline shape with 16 heads, the small-head kernel's bandwidth-bound case
+SFA_H16 = W("sfa_h16", B=64, Q=1, h=16, S=32768, top_k=2048, n_splits=1, index_kind="uniform", seed=1234 + 6)
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -96,6 +113,22 @@ def test_full_size_every_element(name):
         uo, ul = run_cuda(inp, n_splits=1)
         compare(uo, ul, ro, rl, name + " unsplit")
     assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("path", [0, 2], ids=["small_head", "pair"])
+def test_full_size_small_head_every_element(path):
+    """B=64, h=16, top_k=2048 over S=32768 on both tcgen05 kernels, every element."""
+    prev = sfa.set_kernel_path(path)
+    try:
+        inp = workloads.make(SFA_H16, device="cuda")
+        assert sfa.decode_launches(64, 1, 16, 2048, 64, 1)[1] == (2 if path == 0 else 1)
+        out, lse = run_cuda(inp)
+        torch.cuda.synchronize()
+        ro, rl = oracle.decode(problem_of(inp))
+        compare(out, lse, ro, rl, "sfa_h16 every element")
+        assert sfa.last_device_status() == 0
+    finally:
+        sfa.set_kernel_path(prev)
 
 
 # ------------------------------------------------------------------------------------------
@@ -291,6 +324,30 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     ro, rl = oracle.decode(problem_of(inp))
     out, lse = run_cuda(inp)
     compare(out, lse, ro, rl, "after timeout")
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("h,B", [(16, 2), (32, 64)])
+def test_small_head_kernel_timeout_is_reported_and_context_survives(h, B):
+    # the small-head kernel with a stalled wait, alone (B=2: clusters of 4) and with clusters
+    # of 2: it reports the timeout, every CTA of a cluster still reaches the cluster
+    # barriers, and the next call is exact
+    w = W("timeout_small", B=B, Q=1, h=h, S=4096, top_k=512, n_splits=1, index_kind="uniform", seed=31)
+    inp = workloads.make(w, device="cuda")
+    assert sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1] == 2
+    sfa.last_device_status()
+    prev = sfa.set_wait_limit(1000)
+    prev_stall = sfa.set_stall_injection(True)
+    try:
+        run_cuda(inp)
+        status = sfa.last_device_status()
+    finally:
+        sfa.set_stall_injection(prev_stall)
+        sfa.set_wait_limit(prev)
+    assert status == -5
+    ro, rl = oracle.decode(problem_of(inp))
+    out, lse = run_cuda(inp)
+    compare(out, lse, ro, rl, "small-head kernel after timeout")
     assert sfa.last_device_status() == 0
 
 
