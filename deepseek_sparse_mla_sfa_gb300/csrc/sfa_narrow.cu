@@ -66,8 +66,11 @@ constexpr int kPBuffers = 2;                      // tile i's P in buffer i % 2
 constexpr int kOffList = kOffP + kPBuffers * kPBytes;
 constexpr int kListCap = 43 * kNt;                // resolved rows kept at once (whole tiles)
 constexpr int kOffMisc = kOffList + kListCap * 4;
-// misc: per-head (m, l) [32] float2, rescale factors [32], output scales [32], flags
-constexpr int kMiscBytes = 32 * 8 + 32 * 4 + 32 * 4 + 64 + 4 * kWarps;   // flags: [0] rescale, [1] abort, [2] stop
+// misc: per-head (m, l) [32] float2 (+0), rescale factors [32] (+256), the warps' partial
+// maxima [2 tile parities][4 warps][32] (+384), output scales [32] (+1408), the warps'
+// partial sums [4][32] (+1536), flags (+2048: [0] rescale, [1] abort, [2] stop), the TMEM
+// address (+2064), per-warp counts (+2112)
+constexpr int kMiscBytes = 2112 + 4 * kWarps;
 constexpr int kOffBar = (kOffMisc + kMiscBytes + 7) / 8 * 8;
 constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQLoad = kBarKvEmpty + kStages,
               kBarQReady = kBarQLoad + 1, kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2,
@@ -104,10 +107,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* list_s = reinterpret_cast<int*>(smem + kOffList);
   float2* ml_s = reinterpret_cast<float2*>(smem + kOffMisc);                   // [32] (m, l)
   float* alpha_s = reinterpret_cast<float*>(smem + kOffMisc + 256);           // [32]
-  float* scale_s = reinterpret_cast<float*>(smem + kOffMisc + 384);           // [32]
-  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 512);  // [0] rescale, [1] abort
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + 520);
-  int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 576);              // [kWarps]
+  float* mxs_base = reinterpret_cast<float*>(smem + kOffMisc + 384);          // [2][4][32]
+  float* scale_s = reinterpret_cast<float*>(smem + kOffMisc + 1408);          // [32]
+  float* lpart_s = reinterpret_cast<float*>(smem + kOffMisc + 1536);          // [4][32]
+  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 2048);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + 2064);
+  int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 2112);             // [kWarps]
   volatile int* abort_s = flags_s + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,10 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarKvEmpty + s], 1);
     }
     mbar_init(&bars[kBarQLoad], 1);
-    mbar_init(&bars[kBarQReady], 1);
+    mbar_init(&bars[kBarQReady], 4);        // one arrival per warp 0-3 (each holds a copy of q)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kBarSFull + x], 1);   // QK^T of the tile in this score buffer done
-      mbar_init(&bars[kBarSFree + x], 1);   // the softmax read this score buffer
+      mbar_init(&bars[kBarSFree + x], 4);   // the four softmax warps read this score buffer
     }
     for (int x = 0; x < kPBuffers; ++x) {
       mbar_init(&bars[kBarPReady + x], 4);  // P in this buffer and O rescaled (one arrival per warp 0-3)
@@ -150,9 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     flags_s[2] = 0;
     *abort_s = 0;
     fence_barrier_init();
-    // q's rope columns of this token as the shared-memory A operand of the rope steps
-    mbar_arrive_expect_tx(&bars[kBarQLoad], (uint32_t)(np.q_rows * 128));
-    tma_load_3d(smem_u32(smem + kOffQRope), &tmap_qrope, 512, 0, t, &bars[kBarQLoad]);
+    // q's rope columns of this token as the shared-memory A operand of the rope steps, in
+    // each 32-row group (rows 32w + head), matching the four copies of q in TMEM
+    mbar_arrive_expect_tx(&bars[kBarQLoad], (uint32_t)(4 * np.q_rows * 128));
+    for (int w = 0; w < 4; ++w)
+      tma_load_3d(smem_u32(smem + kOffQRope + w * 32 * 128), &tmap_qrope, 512, 0, t, &bars[kBarQLoad]);
   }
   if (warp == 0) {
     tmem_alloc(tmem_base_s, kTmemCols);
@@ -214,14 +221,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, wl));
   };
 
-  float m_ref = -INFINITY, l_sum = 0.f;   // warp 0: running max (log2 units) and sum of head `lane`
+  // warps 0-3: running max of head `lane` (log2 units, the same in every warp) and this
+  // warp's share of its running sum (the four shares are added at the end)
+  float m_ref = -INFINITY, l_part = 0.f;
   if (warp < 4) {
-    // =================== softmax (warp 0) / O rescale (warps 0-3) ===================
+    // =================== softmax and O rescale (warps 0-3) ==========================
+    // q's rows are replicated in the four TMEM lane quadrants (and the four 32-row groups
+    // of the rope operand), so every warp sees every head's scores; warp w takes tile
+    // columns 12w..12w+11.
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const int head = lane;   // warp 0 only
-    if (warp == 0) {
-      // q's latent columns of head `lane` into TMEM as bf16 pairs (the A operand of the
-      // latent steps of QK^T); lanes past h hold zeros
+    const int head = lane;
+    {
+      // q's latent columns of head `lane` into this warp's quadrant as bf16 pairs (the A
+      // operand of the latent steps of QK^T); lanes past h hold zeros
       const bool have = lane < p.h;
       const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.h + (have ? lane : 0)) * kDQK);
 #pragma unroll 1
@@ -247,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float c_scale = p.scale * kLog2e;
     const float c_abs = fabsf(c_scale);
-    char* p_row0 = smem + kOffP + head * 128;   // this head's row of the P^T tiles
+    constexpr int kCols = kNt / 4;   // tile columns per warp
+    const int col0 = warp * kCols;
     // Warps 0-3 leave the tile loop together: warp 0 alone reads the abort flag at the top
     // of each tile and publishes the decision before the barrier the others wait at.
     for (int i = 0; i < n_local; ++i) {
@@ -255,97 +268,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 0) {
         bool go = !*abort_s;
         if (go && !wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); go = false; }
-        if (go) {
-          tc_fence_after();
-          uint32_t v[3][16];
-#pragma unroll
-          for (int c = 0; c < 3; ++c) tmem_ld16(lane_base + kColS + 64 * bb + 16 * c, v[c]);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarSFree + bb]);
-          float s[kNt];
-#pragma unroll
-          for (int j = 0; j < kNt; ++j) s[j] = __uint_as_float(v[j >> 4][j & 15]);
-          const int g = (int)crank + (int)G * i;   // the unit's tile index
-          const int nvalid = min(kNt, total - kNt * g);
-          if (c_scale < 0.f) {   // keep max(s) * |c| == max(s * c) for a negative scale
-#pragma unroll
-            for (int j = 0; j < kNt; ++j) s[j] = -s[j];
-          }
-#pragma unroll
-          for (int j = 0; j < kNt; ++j)
-            if (j >= nvalid || head >= p.h) s[j] = -INFINITY;
-          float mx[12];
-#pragma unroll
-          for (int j = 0; j < 12; ++j) mx[j] = fmaxf(fmaxf(s[4 * j], s[4 * j + 1]), fmaxf(s[4 * j + 2], s[4 * j + 3]));
-#pragma unroll
-          for (int j = 0; j < 6; ++j) mx[j] = fmaxf(mx[j], mx[j + 6]);
-          const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(mx[4], mx[5])) * c_abs;
-          float m_new = m_ref;
-          if (head < p.h && (i == 0 || mt > m_ref + kRescaleThreshold)) m_new = fmaxf(mt, m_ref);
-          const float alpha = (i == 0 || head >= p.h) ? 1.f : ex2(m_ref - m_new);
-          m_ref = m_new;
-          uint32_t pk[kNt / 2];
-          float sm = 0.f;
-#pragma unroll
-          for (int j = 0; j < kNt / 2; ++j) {
-            const float e0 = head < p.h ? ex2(fmaf(s[2 * j], c_abs, -m_new)) : 0.f;
-            const float e1 = head < p.h ? ex2(fmaf(s[2 * j + 1], c_abs, -m_new)) : 0.f;
-            sm += e0 + e1;
-            pk[j] = pack_bf16(e0, e1);
-          }
-          l_sum = l_sum * alpha + sm;
-          if (lane < NH) alpha_s[lane] = alpha;
-          const bool resc = __any_sync(0xffffffffu, alpha != 1.f);
-          // P buffer bb is free once P.V of tile i-2 has read it
-          if (i >= 2 && !wait_warp(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); go = false; }
-          if (go && lane < NH) {
-            // this head's row of P^T: 48 bf16 in six 16-byte chunks of a K-major SW128 row
-            char* p_row = p_row0 + bb * kPBytes;
-#pragma unroll
-            for (int c = 0; c < kNt / 8; ++c)
-              *reinterpret_cast<uint4*>(p_row + ((c ^ (head & 7)) * 16)) =
-                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            fence_proxy_async_smem();
-          }
-          // O is rescaled (rarely: the reference max moves only by more than the threshold)
-          // once P.V of the previous tile has completed; warps 1-3 learn it at the barrier.
-          // (Tile i+1 waits on the same phase of that buffer again: it cannot have moved on,
-          // P.V of tile i+1 is not issued before then.)
-          if (go && resc && i >= 1 && !wait_warp(&bars[kBarPFree + (bb ^ 1)], ((i - 1) >> 1) & 1)) {
-            fail();
-            go = false;
-          }
-          if (lane == 0) flags_s[0] = resc ? 1 : 0;
-        }
+        // P buffer bb is free once P.V of tile i-2 has read it
+        if (go && i >= 2 && !wait_warp(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); go = false; }
         if (lane == 0) flags_s[2] = go ? 0 : 1;
       }
-      // warps 1-3 learn whether to stop and whether O is rescaled
-      named_barrier(1, 128);
+      named_barrier(1, 128);   // A: the scores of tile i are in TMEM and P buffer bb is free
       if (flags_s[2]) break;
       tc_fence_after();
-      if (flags_s[0]) {
+      uint32_t v[16];
+      tmem_ld16(lane_base + kColS + 64 * bb + col0, v);   // columns col0 .. col0+11 used
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarSFree + bb]);
+      float s[kCols];
+      const int g = (int)crank + (int)G * i;   // the unit's tile index
+      const int nvalid = min(kNt, total - kNt * g);
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) {
+        float x = __uint_as_float(v[j]);
+        if (c_scale < 0.f) x = -x;   // keep max(s) * |c| == max(s * c) for a negative scale
+        s[j] = (col0 + j >= nvalid || head >= p.h) ? -INFINITY : x;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int j = 1; j < kCols; ++j) mx = fmaxf(mx, s[j]);
+      float* mx_s = mxs_base + 128 * bb;   // [4 warps][32 heads] of this tile parity
+      mx_s[warp * 32 + lane] = mx;
+      named_barrier(2, 128);   // B: every warp's partial max of tile i is published
+      const float mt = fmaxf(fmaxf(mx_s[lane], mx_s[32 + lane]), fmaxf(mx_s[64 + lane], mx_s[96 + lane])) * c_abs;
+      float m_new = m_ref;
+      if (head < p.h && (i == 0 || mt > m_ref + kRescaleThreshold)) m_new = fmaxf(mt, m_ref);
+      const float alpha = (i == 0 || head >= p.h) ? 1.f : ex2(m_ref - m_new);
+      m_ref = m_new;
+      uint32_t pk[kCols / 2];
+      float sm = 0.f;
+#pragma unroll
+      for (int j = 0; j < kCols / 2; ++j) {
+        const float e0 = head < p.h ? ex2(fmaf(s[2 * j], c_abs, -m_new)) : 0.f;
+        const float e1 = head < p.h ? ex2(fmaf(s[2 * j + 1], c_abs, -m_new)) : 0.f;
+        sm += e0 + e1;
+        pk[j] = pack_bf16(e0, e1);
+      }
+      l_part = l_part * alpha + sm;
+      if (lane < NH) {
+        // this head's row of P^T, tile columns col0..col0+11 = bytes 24w..24w+23 of the
+        // K-major SW128 row: three 8-byte pieces, none crossing a 16-byte chunk
+        char* p_row = smem + kOffP + bb * kPBytes + head * 128;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          const int byte = 2 * col0 + 8 * u;
+          *reinterpret_cast<uint2*>(p_row + ((((byte >> 4) ^ (head & 7)) << 4) | (byte & 15))) =
+              make_uint2(pk[2 * u], pk[2 * u + 1]);
+        }
+        fence_proxy_async_smem();
+      }
+      if (warp == 0) {
+        // O is rescaled (rarely: the reference max moves only by more than the threshold)
+        // once P.V of the previous tile has completed.  (Tile i+1 waits on the same phase
+        // of that buffer again: it cannot have moved on, P.V of tile i+1 is not issued yet.)
+        const bool resc = __any_sync(0xffffffffu, alpha != 1.f);
+        if (resc && i >= 1 && !wait_warp(&bars[kBarPFree + (bb ^ 1)], ((i - 1) >> 1) & 1)) fail();
+        if (lane < NH) alpha_s[lane] = alpha;
+        if (lane == 0) flags_s[0] = resc ? 1 : 0;
+      }
+      named_barrier(3, 128);   // C: whether O is rescaled, and by what
+      if (flags_s[0] && !*abort_s) {
+        tc_fence_after();
         // O^T lane v holds output column v of every head: scale column hh by alpha[hh]
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
 #pragma unroll
           for (int c16 = 0; c16 < NH / 16; ++c16) {
-            uint32_t v[16];
-            tmem_ld16(lane_base + kColO + NH * m + 16 * c16, v);
+            uint32_t o[16];
+            tmem_ld16(lane_base + kColO + NH * m + 16 * c16, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha_s[16 * c16 + k]);
-            tmem_st16(lane_base + kColO + NH * m + 16 * c16, v);
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[16 * c16 + k]);
+            tmem_st16(lane_base + kColO + NH * m + 16 * c16, o);
           }
         }
+        tmem_st_wait();
       }
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarPReady + bb]);
-      // every warp 0-3 has read this tile's flags before warp 0 writes the next tile's
-      named_barrier(3, 128);
     }
   } else if (warp < kProducerWarp + kProducerWarps) {
     // =================== gathers ===================================================
@@ -468,8 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_o = wait_warp(&bars[kBarPvFinal], 0);
       if (!have_o) fail();
     }
-    if (warp == 0)
+    lpart_s[warp * 32 + lane] = l_part;
+    named_barrier(2, 128);
+    if (warp == 0) {
+      const float l_sum = (lpart_s[lane] + lpart_s[32 + lane]) + (lpart_s[64 + lane] + lpart_s[96 + lane]);
       ml_s[lane] = (have_o && lane < p.h) ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+    }
   }
   tc_fence_before();
   cluster_sync();   // every CTA's (m, l) is published
