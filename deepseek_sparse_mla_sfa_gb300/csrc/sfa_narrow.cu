@@ -573,25 +573,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-typedef CUresult (*EncodeTiledFnN)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFnN encode_fn_narrow() {
-  static std::atomic<EncodeTiledFnN> fn{nullptr};
-  EncodeTiledFnN f = fn.load(std::memory_order_acquire);
-  if (f) return f;
-  void* ptr = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return nullptr;
-  f = reinterpret_cast<EncodeTiledFnN>(ptr);
-  fn.store(f, std::memory_order_release);
-  return f;
-}
-
 template <int NH, bool kIL>
 constexpr auto narrow_kernel() {
   return decode_narrow_kernel<NH, kIL>;

@@ -35,6 +35,9 @@ INTERLEAVED = [
        block_size=16, seed=34), [5, 64]),
     (W("il_h128_k3000", B=1, Q=1, h=128, S=8192, top_k=3000, n_splits=2, index_kind="uniform",
        seed=35), [32]),
+    # more (token, shard) pairs than CTA pairs: the CTA-pair kernel takes groups of shards
+    (W("il_h128_groups", B=20, Q=1, h=128, S=8000, top_k=600, n_splits=8, index_kind="uniform",
+       seed=36), [16, 1000]),
 ]
 CASES = [(w, g) for w, gs in INTERLEAVED for g in gs]
 

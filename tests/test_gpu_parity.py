@@ -52,6 +52,12 @@ SMALL = [
     W("h8_one_tile", B=2, Q=1, h=8, S=500, top_k=40, n_splits=1, index_kind="uniform", seed=43),
     W("h12_mtp_splits", B=5, Q=2, h=12, S=2500, S_min=30, top_k=400, n_splits=3, index_kind="causal", seed=44),
     W("h2_bs16_g1", B=40, Q=1, h=2, S=900, top_k=300, n_splits=2, index_kind="uniform", block_size=16, seed=45),
+    # CTA-pair kernel with more (token, shard) pairs than CTA pairs: a unit takes a group of
+    # a token's shards (one group per token; two groups per token, with empty shards)
+    W("h128_groups1", B=40, Q=1, h=128, S=4096, top_k=600, n_splits=4, index_kind="uniform", seed=46),
+    W("h128_groups2_dcp", B=30, Q=1, h=128, S=20000, recent=2000, top_k=512, n_splits=8,
+      index_kind="dcp_long", seed=47),
+    W("h64_groups_mtp", B=20, Q=2, h=64, S=6000, S_min=40, top_k=700, n_splits=3, index_kind="causal", seed=48),
 ]
 
 # which kernel decode_launches reports per kernel-path setting (0 automatic, 1 CUDA-core,
