@@ -6,6 +6,9 @@ and the output layout (ascending positions, -1 padded) make the answer unique.
   candidate count, k = 1, empty and short causal ranges, row strides above S;
 * the three top-2048 workloads at full size (every element: the oracle sorts each row);
 * the largest supported row (SFA_TOPK_MAX_S);
+* the sampled threshold and its fallback to the sweep: chunks whose thresholds differ,
+  rows whose top keys crowd the last chunks, negative thresholds, candidates that
+  overflow the cluster's buffer;
 * the chain into decode: sfa_topk's lists drive sfa_decode to the oracle's attention.
 """
 import numpy as np
@@ -109,9 +112,10 @@ def test_topk_lists_drive_decode_to_the_oracle():
 
 @pytest.mark.parametrize("kind", ["ties", "all_equal"])
 def test_full_chunks_with_heavy_ties(kind):
-    """Rows held by one CTA each (enough tokens to fill the GPU), where so many keys tie at
-    the threshold that the per-warp candidate lists overflow and the kernel falls back to
-    sweeping the whole chunk; all-equal rows take the first k positions."""
+    """Rows held by one CTA each (enough tokens to fill the GPU).  Five-valued scores: a
+    fifth of each row ties at the threshold, resolved by position.  All-equal rows: every
+    key is a candidate, the lists overflow, and the sweep's per-warp lists overflow too, so
+    it compacts the whole chunk; they take the first k positions."""
     T, S, k = 160, 32768, 2048
     if kind == "ties":
         sc = workloads.indexer_scores(T, S, "cuda", seed=21, kind="ties")
@@ -120,3 +124,37 @@ def test_full_chunks_with_heavy_ties(kind):
     g = _check(sc, k, S=S, what=kind)
     if kind == "all_equal":
         assert np.array_equal(g, np.tile(np.arange(k, dtype=np.int32), (T, 1)))
+
+
+def _drifting_normal(T, S, seed, drift):
+    """N(0, 1) scores whose mean rises linearly by `drift` along the row."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    x = torch.randn((T, S), generator=gen, device="cuda")
+    if drift:
+        x += torch.linspace(0.0, drift, S, device="cuda")
+    return x
+
+
+# (name, T, S, k, drift): the kernel first lists the keys above a threshold estimated from a
+# sample of each chunk and falls back to sweeping the chunks when that estimate cannot hold
+SAMPLED = [
+    # 8 CTAs per row whose chunks differ in mean: their thresholds differ, the largest still holds
+    ("drift_mild_8_ctas", 6, 65536, 2048, 0.3),
+    # the top keys crowd into the last chunks: fewer than k keys reach the largest threshold
+    ("drift_strong_8_ctas", 6, 65536, 2048, 4.0),
+    # k above half the row: the threshold key is below that of +0
+    ("negative_threshold", 200, 8000, 5000, 0.0),
+    ("small_k_long_row", 4, 30000, 64, 0.0),
+    # the cluster's candidates exceed one chunk's buffer
+    ("candidates_overflow", 8, 32768, 20000, 0.0),
+    # rows of one CTA each (enough tokens to fill the GPU) whose estimate fails: the sweep
+    # without a cluster
+    ("drift_strong_one_cta", 160, 32768, 2048, 4.0),
+]
+
+
+@pytest.mark.parametrize("name,T,S,k,drift", SAMPLED, ids=[c[0] for c in SAMPLED])
+def test_sampled_threshold_and_its_fallback(name, T, S, k, drift):
+    sc = _drifting_normal(T, S, sum(map(ord, name)), drift)
+    _check(sc, k, what=name)
