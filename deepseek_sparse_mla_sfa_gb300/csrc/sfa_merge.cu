@@ -147,9 +147,11 @@ cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int warps_per_block = 8;
+  // small blocks (one warp a row, two rows a block) spread the rows evenly over the SMs:
+  // with eight-warp blocks a short merge gave some SMs a third more rows than others
+  const int warps_per_block = 2;
   long long blocks = ((long long)rows + warps_per_block - 1) / warps_per_block;
-  const long long cap = (long long)sms * 8;
+  const long long cap = (long long)sms * 32;   // resident 64-thread blocks per SM
   if (blocks > cap) blocks = cap;
   const bool vec4 = (dv % 4) == 0;
   const bool fast = dv == 512 && n_splits <= kFastShards && (reinterpret_cast<uintptr_t>(out_part) % 16) == 0 &&
