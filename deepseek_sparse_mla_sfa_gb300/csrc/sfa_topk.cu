@@ -924,7 +924,7 @@ void topk_plan(int T, int S, int n_sms, int& C, int& chunk, int& threads) {
   C = (S + kTopkChunkMax - 1) / kTopkChunkMax;
   if (C < 1) C = 1;
   if (C > 8) C = 8;
-  while (C < 8 && 2LL * T * C <= n_sms && (S + 2 * C - 1) / (2 * C) >= 4096) C *= 2;
+  while (2 * C <= 8 && 2LL * T * C <= n_sms && (S + 2 * C - 1) / (2 * C) >= 4096) C *= 2;
   const int per = (S + C - 1) / C;
   chunk = ((per + kChunkUnit - 1) / kChunkUnit) * kChunkUnit;
   if (chunk < kChunkUnit) chunk = kChunkUnit;
