@@ -47,13 +47,16 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
     // weight of shard r: exp(lse_r - L) (exactly 0 for an empty shard)
     const float w0 = lane < n ? expf(l0 - L) : 0.f;
     const float w1 = lane + 32 < n ? expf(l1 - L) : 0.f;
+    // The column loops run the same trip count on every lane (the weight of shard r comes
+    // from lane r % 32 by a full-warp shuffle); each lane bounds its own column.
     if (kVec4) {
       const int dv4 = dv >> 2;
-      for (int c = lane; c < dv4; c += 32) {
+      for (int c0 = 0; c0 < dv4; c0 += 32) {
+        const int c = c0 + lane;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r = 0; r < n; ++r) {
           const float w = __shfl_sync(0xffffffffu, r < 32 ? w0 : w1, r & 31);
-          if (w == 0.f) continue;
+          if (w == 0.f || c >= dv4) continue;
           const float4 v =
               __ldg(reinterpret_cast<const float4*>(out_part + ((size_t)r * rows + row) * dv) + c);
           acc.x += w * v.x;
@@ -61,17 +64,18 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict_
           acc.z += w * v.z;
           acc.w += w * v.w;
         }
-        reinterpret_cast<float4*>(orow)[c] = acc;
+        if (c < dv4) reinterpret_cast<float4*>(orow)[c] = acc;
       }
     } else {
-      for (int c = lane; c < dv; c += 32) {
+      for (int c0 = 0; c0 < dv; c0 += 32) {
+        const int c = c0 + lane;
         float acc = 0.f;
         for (int r = 0; r < n; ++r) {
           const float w = __shfl_sync(0xffffffffu, r < 32 ? w0 : w1, r & 31);
-          if (w == 0.f) continue;
+          if (w == 0.f || c >= dv) continue;
           acc += w * out_part[((size_t)r * rows + row) * dv + c];
         }
-        orow[c] = acc;
+        if (c < dv) orow[c] = acc;
       }
     }
     if (lane == 0) lse[row] = L;

@@ -120,3 +120,125 @@ def test_topk_random_shapes(seed):
     assert bad.size == 0, (f"seed {seed} (S={S} T={T} k={k} kind={kind} stride={stride} Q={Q} "
                            f"causal={causal}): {bad.shape[0]} entries differ, first at {bad[0].tolist()}")
     assert sfa.last_device_status() == 0
+
+
+def _grid_case(seed):
+    """Batches with more (token, shard) units than the GPU has CTA pairs."""
+    rng = np.random.default_rng(8000 + seed)
+    h = int(rng.choice([16, 32, 64, 128]))
+    B = int(rng.integers(20, 41))
+    Q = int(rng.choice([1, 2]))
+    n_splits = int(rng.choice([1, 2, 4, 8]))
+    S = int(rng.integers(500, 20001))
+    top_k = int(rng.integers(64, 601))
+    kind = str(rng.choice(["uniform", "causal"]))
+    kw = {"S_min": int(rng.integers(0, S + 1))} if kind == "causal" else {}
+    w = workloads.Workload(f"grid{seed}", B=B, Q=Q, h=h, S=S, top_k=top_k, n_splits=n_splits,
+                           index_kind=kind, block_size=int(rng.choice([16, 64])), seed=9000 + seed, **kw)
+    return w, rng
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_decode_random_multi_wave_grids(seed):
+    w, rng = _grid_case(seed)
+    inp = workloads.make(w, device="cuda")
+    per_token = bool(rng.integers(0, 2))
+    bt = workloads.per_token_block_table(inp, seed=seed) if per_token else inp.block_table
+    prob = oracle.Problem(inp.q, inp.kv, bt, inp.seq_lens, inp.topk_idx, w.Q, w.scale)
+    out, lse = sfa.decode(inp.q, inp.kv, bt, inp.seq_lens, inp.topk_idx, w.scale, n_splits=w.n_splits,
+                          Q=w.Q, block_table_per_token=per_token)
+    torch.cuda.synchronize()
+    if per_token:
+        ref_out, ref_lse = oracle.decode_ex(prob, 1, bt_per_token=True)
+        ref_out, ref_lse = ref_out[0], ref_lse[0]
+    else:
+        ref_out, ref_lse = oracle.decode(prob)
+    compare(out, lse, ref_out, ref_lse, f"seed {seed}: {w} per_token={per_token}")
+    assert sfa.last_device_status() == 0
+
+
+@pytest.fixture(params=[1, 2], ids=["cudacore", "pair"])
+def forced_path(request):
+    prev = sfa.set_kernel_path(request.param)
+    yield request.param
+    sfa.set_kernel_path(prev)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_decode_random_shapes_forced_paths(seed, forced_path):
+    """The same random shapes on the CUDA-core kernel and, for h <= 32, on the CTA-pair
+    kernel (which the automatic choice gives only to h > 32)."""
+    w, g, rng = _decode_case(seed)
+    if forced_path == 2 and w.h > 32:
+        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 32")
+    inp = workloads.make(w, device="cuda")
+    inp.topk_idx = _salt_indices(inp, rng)
+    ref_out, ref_lse = oracle.decode(problem_of(inp))
+    out, lse = sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                          n_splits=w.n_splits, Q=w.Q, interleave=g)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_out, ref_lse, f"seed {seed} path {forced_path}: {w} interleave={g}")
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_lse_merge_random(seed):
+    """Shard counts 1 .. 64, row widths with and without 16-byte vectors, empty shards and
+    rows whose every shard is empty."""
+    rng = np.random.default_rng(11000 + seed)
+    n = int(rng.choice([1, 2, 3, 8, 9, 64]))
+    rows = int(rng.integers(1, 700))
+    dv = int(rng.choice([512, 512, 128, 511, 3, 1]))
+    op = rng.standard_normal((n, rows, dv)).astype(np.float32)
+    lp = (3.0 * rng.standard_normal((n, rows))).astype(np.float32)
+    lp[rng.random((n, rows)) < 0.2] = -np.inf              # empty shards
+    lp[:, rng.random(rows) < 0.05] = -np.inf                # rows with no shard at all
+    op[np.isneginf(lp)] = 0.0                               # an empty shard's partial is zero
+    out, lse = sfa.lse_merge(torch.from_numpy(op).cuda(), torch.from_numpy(lp).cuda())
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.merge(op, lp)
+    compare(out, lse, ref_out, ref_lse, f"seed {seed}: n={n} rows={rows} dv={dv}", atol_out=1e-4,
+            atol_lse=1e-4)
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_kv_write_random(seed):
+    rng = np.random.default_rng(12000 + seed)
+    bs = int(rng.choice([1, 16, 64, 256]))
+    num_blocks = int(rng.integers(1, 80))
+    num_slots = num_blocks * bs
+    T = int(rng.integers(0, min(num_slots, 500) + 1))
+    g = torch.Generator().manual_seed(13000 + seed)
+    kv = torch.randn((num_blocks, bs, 576), generator=g).to(torch.bfloat16)
+    rows = torch.randn((T, 576), generator=g).to(torch.bfloat16)
+    slots = torch.from_numpy(rng.permutation(num_slots)[:T].astype(np.int32))
+    if T:
+        slots[torch.from_numpy(rng.random(T) < 0.1)] = -1
+    expect = oracle.kv_write(kv, slots.numpy(), rows)
+    kv_d = kv.cuda()
+    sfa.kv_write(kv_d, slots.cuda(), rows.cuda())
+    torch.cuda.synchronize()
+    got = kv_d.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, expect), f"seed {seed}: bs={bs} blocks={num_blocks} T={T}"
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_uv_proj_random(seed):
+    """Within the rounding bound of the W_UV tests: out rounded to bf16, fp32 sums, y
+    rounded to bf16."""
+    rng = np.random.default_rng(14000 + seed)
+    T = int(rng.integers(1, 300))
+    h = int(rng.integers(1, 129))
+    g = torch.Generator().manual_seed(15000 + seed)
+    out = (0.3 * torch.randn((T, h, 512), generator=g)).float()
+    w = (torch.randn((h, 512, 128), generator=g) / 512 ** 0.5).to(torch.bfloat16)
+    y = sfa.uv_proj(out.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    ref = oracle.uv_proj(out.double().numpy(), w)
+    absprod = np.einsum("thc,hcv->thv", np.abs(out.double().numpy()), np.abs(w.double().numpy()))
+    err = np.abs(y.double().cpu().numpy() - ref)
+    bound = 2.0 ** -8 * absprod + 2.0 ** -8 * np.abs(ref) + 1e-6
+    assert np.all(err <= bound), f"seed {seed}: T={T} h={h} max err/bound {np.max(err / bound):.3f}"
+    assert sfa.last_device_status() == 0
