@@ -258,7 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[kBarQReady]);
     }
     const float c_scale = p.scale * kLog2e;
-    const float c_abs = fabsf(c_scale);
+    // |scale| in log2 units, at least 1e-30: masked scores are -inf, and -inf times a zero
+    // scale would be NaN.  For a zero scale every valid weight still rounds to exactly 1
+    // (|scores * 1e-30| is far below one ulp of 1), the uniform average the definition gives.
+    const float c_abs = fmaxf(fabsf(c_scale), 1e-30f);
     constexpr int kCols = kNt / 4;   // tile columns per warp
     const int col0 = warp * kCols;
     // Warps 0-3 leave the tile loop together: warp 0 alone reads the abort flag at the top

@@ -314,7 +314,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 
     const float c_scale = p.scale * kLog2e;
-    const float c_abs = fabsf(c_scale);
+    // |scale| in log2 units, at least 1e-30: masked scores are -inf, and -inf times a zero
+    // scale would be NaN.  For a zero scale every valid weight still rounds to exactly 1
+    // (|scores * 1e-30| is far below one ulp of 1), the uniform average the definition gives.
+    const float c_abs = fmaxf(fabsf(c_scale), 1e-30f);
     const char* xin = smem + kOffX + head * 256;   // the peer's partial scores of this head
 
     float m_ref = -INFINITY, l_sum = 0.f;  // running max (log2 units) and sum of this head

@@ -242,3 +242,74 @@ def test_uv_proj_random(seed):
     bound = 2.0 ** -8 * absprod + 2.0 ** -8 * np.abs(ref) + 1e-6
     assert np.all(err <= bound), f"seed {seed}: T={T} h={h} max err/bound {np.max(err / bound):.3f}"
     assert sfa.last_device_status() == 0
+
+
+def _decode_case_b(seed):
+    """Any head count, block sizes that are not powers of two, long lists (the CTA-pair
+    kernel keeps 2048 resolved entries at a time) and scales of either sign around the
+    configurations' 1/sqrt(192)."""
+    rng = np.random.default_rng(16000 + seed)
+    h = int(rng.integers(1, 129))
+    B = int(rng.integers(1, 5))
+    Q = int(rng.choice([1, 2]))
+    bs = int(rng.choice([2, 3, 5, 48, 100, 128, 1000, 64]))
+    kind = str(rng.choice(["uniform", "causal"]))
+    S = int(rng.integers(1, 9001))
+    top_k = int(rng.choice([int(rng.integers(1, 300)), int(rng.integers(2048, 6001))]))
+    n_splits = int(rng.choice([1, 2, 4]))
+    scale = float(rng.choice([1.0, -1.0, 0.0, 0.5, 2.0])) * workloads.SCALE
+    kw = {"S_min": int(rng.integers(0, S + 1))} if kind == "causal" else {}
+    w = workloads.Workload(f"fuzzb{seed}", B=B, Q=Q, h=h, S=S, top_k=top_k, n_splits=n_splits,
+                           index_kind=kind, block_size=bs, seed=17000 + seed, scale=scale, **kw)
+    return w, rng
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_decode_random_shapes_b(seed):
+    w, rng = _decode_case_b(seed)
+    inp = workloads.make(w, device="cuda")
+    inp.topk_idx = _salt_indices(inp, rng)
+    prob = problem_of(inp)
+    ref_out, ref_lse = oracle.decode(prob)
+    out, lse = sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                          n_splits=w.n_splits, Q=w.Q)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_out, ref_lse, f"seed {seed}: {w}")
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_decode_noalloc_and_host_entry_points_random(seed):
+    """The no-allocation and host-buffer entry points on random shapes, against the oracle."""
+    w, g, rng = _decode_case(100 + seed)
+    inp = workloads.make(w, device="cuda")
+    ref_out, ref_lse = oracle.decode(problem_of(inp))
+    out, lse = sfa.decode_noalloc(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                                  n_splits=w.n_splits, Q=w.Q)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_out, ref_lse, f"noalloc seed {seed}: {w}")
+    pin = lambda t: t.cpu().contiguous().pin_memory()
+    out_h = torch.full((w.T, w.h, 512), float("nan"), dtype=torch.float32).pin_memory()
+    lse_h = torch.full((w.T, w.h), float("nan"), dtype=torch.float32).pin_memory()
+    nbytes = sfa.decode_host_staging_bytes(w.B, w.Q, w.h, w.top_k, inp.max_blocks, w.n_splits)
+    staging = torch.empty(max(1, nbytes), dtype=torch.uint8, device="cuda")
+    sfa.decode_host(pin(inp.q), inp.kv, pin(inp.block_table), pin(inp.seq_lens), pin(inp.topk_idx),
+                    w.scale, w.n_splits, w.Q, out_h, lse_h, staging)
+    torch.cuda.synchronize()
+    compare(out_h, lse_h, ref_out, ref_lse, f"host seed {seed}: {w}")
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("S,T", [(98305, 2), (163841, 1), (196609, 3), (229377, 2), (131073, 40),
+                                 (65537, 76), (32769, 77), (40000, 3)])
+def test_topk_odd_cluster_sizes(S, T):
+    """Rows whose plan is a cluster of 3, 5, 6, 7 or 8 CTAs (or 2 at the grid's edge), with
+    k around 1 % and 50 % of the row (a threshold key below that of +0)."""
+    for k in (max(1, S // 100), S // 2):
+        sc = workloads.indexer_scores(T, S, "cuda", seed=S + T + k)
+        got = sfa.topk(sc, k, S=S)
+        torch.cuda.synchronize()
+        ref = oracle.topk(sc, k, S=S)
+        bad = np.argwhere(got.cpu().numpy() != ref)
+        assert bad.size == 0, f"S={S} T={T} k={k}: {bad.shape[0]} entries differ, first at {bad[0].tolist()}"
+    assert sfa.last_device_status() == 0
