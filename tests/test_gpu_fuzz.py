@@ -313,3 +313,67 @@ def test_topk_odd_cluster_sizes(S, T):
         bad = np.argwhere(got.cpu().numpy() != ref)
         assert bad.size == 0, f"S={S} T={T} k={k}: {bad.shape[0]} entries differ, first at {bad[0].tolist()}"
     assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_decode_rescale_stress(seed):
+    """q scaled up (scores spread over tens of log2 units) and each list sorted by its
+    score, ascending or descending, so the running max grows on almost every tile (and O is
+    rescaled) or never after the first."""
+    rng = np.random.default_rng(18000 + seed)
+    h = int(rng.choice([4, 16, 32, 64, 128]))
+    w = workloads.Workload(f"stress{seed}", B=2, Q=1, h=h, S=6000, top_k=int(rng.integers(500, 3000)),
+                           n_splits=int(rng.choice([1, 3])), index_kind="uniform", seed=19000 + seed)
+    inp = workloads.make(w, device="cuda")
+    inp.q = (inp.q.float() * float(rng.choice([2.0, 4.0]))).to(torch.bfloat16)
+    prob = problem_of(inp)
+    # order each token's list by the score of its first head
+    kv = inp.kv.float().reshape(-1, 576)
+    q0 = inp.q.float()[:, 0, :]
+    for t in range(w.T):
+        idx = inp.topk_idx[t].long()
+        valid = idx >= 0
+        pos = idx[valid]
+        blk = inp.block_table[t // w.Q, pos // w.block_size].long()
+        rows = kv[blk * w.block_size + pos % w.block_size]
+        sc = rows @ q0[t]
+        order = torch.argsort(sc, descending=bool(seed % 2))
+        inp.topk_idx[t, :pos.numel()] = pos[order].to(torch.int32)
+        inp.topk_idx[t, pos.numel():] = -1
+    prob = problem_of(inp)
+    ref_out, ref_lse = oracle.decode(prob)
+    out, lse = sfa.decode(inp.q, inp.kv, inp.block_table, inp.seq_lens, inp.topk_idx, w.scale,
+                          n_splits=w.n_splits, Q=w.Q)
+    torch.cuda.synchronize()
+    compare(out, lse, ref_out, ref_lse, f"seed {seed}: {w}")
+    assert sfa.last_device_status() == 0
+
+
+@pytest.mark.parametrize("case", ["all_neg_inf", "all_pos_inf", "all_nan", "mixed_inf",
+                                  "short_causal_big_cluster", "one_valid_per_cta"])
+def test_topk_degenerate_rows(case):
+    T, S, k = 4, 70000, 2048
+    Q, seq_lens = 1, None
+    sc = workloads.indexer_scores(T, S, "cuda", seed=77)
+    if case == "all_neg_inf":
+        sc[:, :S] = float("-inf")
+    elif case == "all_pos_inf":
+        sc[:, :S] = float("inf")
+    elif case == "all_nan":
+        sc[:, :S] = float("nan")
+    elif case == "mixed_inf":
+        g = torch.Generator(device="cuda").manual_seed(78)
+        pick = torch.randint(0, 3, (T, S), generator=g, device="cuda")
+        sc[:, :S] = torch.where(pick == 0, float("-inf"), torch.where(pick == 1, float("inf"), sc[:, :S]))
+    elif case == "short_causal_big_cluster":
+        # the rows plan clusters of several CTAs; the causal ranges reach only the first chunk
+        seq_lens = torch.tensor([3000, 2049, 5000, 100], dtype=torch.int32, device="cuda")
+    elif case == "one_valid_per_cta":
+        k = 1
+        seq_lens = torch.tensor([S, 1, 40000, 35000], dtype=torch.int32, device="cuda")
+    got = sfa.topk(sc, k, seq_lens=seq_lens, Q=Q, S=S)
+    torch.cuda.synchronize()
+    ref = oracle.topk(sc, k, seq_lens=seq_lens, Q=Q, S=S)
+    bad = np.argwhere(got.cpu().numpy() != ref)
+    assert bad.size == 0, f"{case}: {bad.shape[0]} entries differ, first at {bad[0].tolist()}"
+    assert sfa.last_device_status() == 0
