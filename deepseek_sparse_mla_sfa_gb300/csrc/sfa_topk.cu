@@ -467,7 +467,7 @@ __device__ __forceinline__ bool sampled_select(const TopkParams& p, const TkRow&
   __syncthreads();
 
   // ---- the k-th largest of the keys at or above tau_max: radix passes over [base, hi]
-  // with 13-bit digits of (key - base) >> s, s set by the range (<= 3 passes, 2 typical)
+  // with 13-bit digits of (key - base) >> s, s set by the range (<= 3 passes, 1-2 typical)
   uint32_t base = tau_max, hi = sh.kmax, krem = (uint32_t)p.k;
   if (hi < base) return false;   // no key reaches tau_max
   uint32_t lo_t = 0u, hi_t = 0u;   // keys above hi_t are chosen, and the first krem in [lo_t, hi_t]
@@ -484,7 +484,7 @@ __device__ __forceinline__ bool sampled_select(const TopkParams& p, const TkRow&
         if (i + x < n_tot && kk[x] >= base && kk[x] <= hi) atomicAdd(&hist[hslot((kk[x] - base) >> s)], 1u);
     }
     __syncthreads();
-    // bins >= nb stay zero; the call leaves every bin zero for the next pass
+    // bins above (hi - base) >> s stay zero; the call leaves every bin zero for the next pass
     const uint32_t tot = find_from_top(hist, krem, sh.wsum, sh.sel);
     if (tot < krem) return false;   // pass 0 only: fewer than k keys reach tau_max
     const uint32_t bin = sh.sel[0], need = sh.sel[1], inbin = sh.sel[2];
