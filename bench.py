@@ -567,7 +567,8 @@ def measure_configs(sfa, peaks, flush, measured_name, measured, measured_acc, st
         if name == "sfa_h16":
             entry["note"] = ("not one of the five workloads: the headline shape with 16 heads, "
                              "where the step is a gather with little arithmetic per byte")
-        entry["kernel"] = {2: "tcgen05 small-head", 1: "tcgen05 CTA pair", 0: "cuda-core"}[
+        entry["kernel"] = {3: "tcgen05 stacked-half", 2: "tcgen05 small-head", 1: "tcgen05 CTA pair",
+                           0: "cuda-core"}[
             sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1]]
         res[name] = entry
     return res

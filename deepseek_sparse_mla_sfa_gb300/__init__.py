@@ -362,7 +362,7 @@ def topk(scores, k: int, seq_lens=None, Q: int = 1, S: Optional[int] = None, out
 
 def decode_launches(B, Q, h, top_k, block_size, n_splits, merge=True):
     """(kernels one decode call enqueues, which kernel serves it: 2 small-head tcgen05,
-    1 CTA-pair tcgen05, 0 CUDA-core)."""
+    3 stacked-half tcgen05, 1 CTA-pair tcgen05, 0 CUDA-core)."""
     tc = ctypes.c_int(0)
     n = int(_lib.load().sfa_decode_launches(B, Q, h, top_k, block_size, n_splits, int(bool(merge)),
                                             ctypes.byref(tc)))
@@ -379,8 +379,9 @@ def last_device_status(stream=None) -> int:
 
 
 def set_kernel_path(path: int) -> int:
-    """0 = automatic (small-head tcgen05 kernel for h <= 32, CTA-pair tcgen05 kernel
-    above), 1 = CUDA-core kernel only, 2 = CTA-pair tcgen05 kernel for every h."""
+    """0 = automatic (small-head tcgen05 kernel for h <= 32, stacked-half tcgen05 kernel
+    for h <= 64, CTA-pair tcgen05 kernel above), 1 = CUDA-core kernel only, 2 = CTA-pair
+    tcgen05 kernel for every h."""
     prev = int(_lib.load().sfa_set_kernel_path(int(path)))
     if prev < 0:
         raise ValueError("path must be 0, 1 or 2")

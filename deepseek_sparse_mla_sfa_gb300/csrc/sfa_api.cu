@@ -26,11 +26,14 @@ std::atomic<long long> g_wait_limit{0};
 std::atomic<int> g_kernel_path{0};  // 0 automatic, 1 CUDA-core only, 2 CTA-pair tcgen05 for every h
 std::atomic<int> g_stall{0};        // test hook: kernels first wait on a barrier nothing completes
 
-// 0: CUDA-core kernel, 1: CTA-pair tcgen05 kernel, 2: small-head tcgen05 kernel
+// 0: CUDA-core kernel, 1: CTA-pair tcgen05 kernel, 2: small-head tcgen05 kernel,
+// 3: stacked-half tcgen05 kernel
 int kernel_choice(int h, int block_size) {
   const int path = g_kernel_path.load();
   if (path == 1 || !sfa::tc_supports(h, block_size)) return 0;
-  return path == 0 && sfa::narrow_supports(h) ? 2 : 1;
+  if (path == 2) return 1;
+  if (sfa::narrow_supports(h)) return 2;
+  return sfa::stack_supports(h) ? 3 : 1;
 }
 constexpr long long kDefaultWaitLimit = 1LL << 26;  // iterations of a bounded device wait
 
@@ -232,7 +235,7 @@ sfa_status sfa_decode_ex(const void* q, const void* kv, const int32_t* block_tab
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int choice = kernel_choice(h, block_size);
   const bool tc = choice != 0 && sfa::tc_supports_ptrs(q, kv, p.out);
-  cudaError_t e = tc ? sfa::launch_decode_tc(p, choice == 2, s) : sfa::launch_decode_simt(p, s);
+  cudaError_t e = tc ? sfa::launch_decode_tc(p, choice, s) : sfa::launch_decode_simt(p, s);
   if (e != cudaSuccess) return SFA_ERR_CUDA;
   if (merge_after) {
     e = sfa::launch_lse_merge(out_part, lse_part, n_splits, T * h, SFA_D_V, out, lse, s);
@@ -383,6 +386,7 @@ sfa_status sfa_host_plan_create(const void* q_host, const void* kv, const int32_
   if (!status_word(dev)) return SFA_ERR_CUDA;
   host_pipe(dev);
   if (sfa::prepare_decode_tc() != cudaSuccess || sfa::prepare_decode_narrow() != cudaSuccess ||
+      sfa::prepare_decode_stack() != cudaSuccess ||
       sfa::prepare_decode_simt() != cudaSuccess)
     return SFA_ERR_CUDA;
   cudaStream_t cs = nullptr;

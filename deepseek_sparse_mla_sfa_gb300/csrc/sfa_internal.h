@@ -110,14 +110,16 @@ cudaError_t launch_kv_write(void* kv, long long num_slots, const int32_t* slot_m
 cudaError_t launch_lse_merge(const float* out_part, const float* lse_part, int n_splits, int rows,
                              int dv, float* out, float* lse, cudaStream_t stream);
 
-// tcgen05 path: whether it handles this problem, its workspace, and its launch.  Two
-// kernels: the CTA-pair kernel (any h <= 128) and the small-head kernel (h <= 32).
+// tcgen05 path: whether it handles this problem, its workspace, and its launch.  Three
+// kernels: the CTA-pair kernel (any h <= 128), the small-head kernel (h <= 32) and the
+// stacked-half kernel (33 <= h <= 64).
 bool tc_supports(int h, int block_size);
 // the tcgen05 path also needs 16-byte aligned q, kv and out (TMA tensor maps)
 bool tc_supports_ptrs(const void* q, const void* kv, const void* out);
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits);
 int tc_launches(int T, int h, int top_k, int n_splits);
-cudaError_t launch_decode_tc(const DecodeParams& p, bool small_heads, cudaStream_t stream);
+// kernel: 1 = CTA pair, 2 = small head, 3 = stacked halves
+cudaError_t launch_decode_tc(const DecodeParams& p, int kernel, cudaStream_t stream);
 // the small-head kernel (sfa_narrow.cu): heads it serves, its one-time set-up, its
 // cluster size for `units` (token, shard) units on n_sms SMs, and its launch with the
 // cache-row map (64 columns x 1 row, 128-byte swizzle) and q's rope map (64 columns x h)
@@ -126,5 +128,13 @@ cudaError_t prepare_decode_narrow();
 int narrow_cluster_size(long long units, int n_sms);
 cudaError_t launch_decode_narrow(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
                                  cudaStream_t stream);
+// the stacked-half kernel (sfa_stack.cu, 33 <= h <= 64): the same maps, one CTA (or a
+// cluster of 2 or 4 when units are few) per unit
+bool stack_supports(int h);
+cudaError_t prepare_decode_stack();
+cudaError_t launch_decode_stack(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
+                                int n_sms, cudaStream_t stream);
+// SM count of the current device (looked up once per device)
+int device_sm_count();
 
 }  // namespace sfa

@@ -581,8 +581,10 @@ constexpr auto narrow_kernel() {
   return decode_narrow_kernel<NH, kIL>;
 }
 
+}  // namespace
+
 // SM count of the current device, looked up once per device
-int sm_count() {
+int device_sm_count() {
   static std::atomic<int> n_sms[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -594,8 +596,6 @@ int sm_count() {
   }
   return n;
 }
-
-}  // namespace
 
 bool narrow_supports(int h) { return h >= 1 && h <= kMaxNarrowHeads; }
 
@@ -620,7 +620,7 @@ cudaError_t prepare_decode_narrow() {
     }
     attr_set[dev].store(true, std::memory_order_release);
   }
-  (void)sm_count();
+  (void)device_sm_count();
   return cudaSuccess;
 }
 
@@ -632,7 +632,7 @@ cudaError_t launch_decode_narrow(const DecodeParams& p, const CUtensorMap& rows_
   const long long num_rows = (long long)p.num_blocks * p.block_size;
   cudaError_t e = prepare_decode_narrow();
   if (e != cudaSuccess) return e;
-  const int G = narrow_cluster_size(units, sm_count());
+  const int G = narrow_cluster_size(units, device_sm_count());
   if (num_rows >= 0x7fffffffLL || units * G > 0x7fffffffLL) return cudaErrorInvalidValue;
   NarrowParams np;
   np.p = p;

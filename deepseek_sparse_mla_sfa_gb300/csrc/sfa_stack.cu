@@ -1,0 +1,690 @@
+// sfa_stack.cu -- tcgen05 / TMA path of sparse MLA decode for 33-64 heads on sm_103a:
+// one CTA per work unit, the two column halves of QK^T stacked in the M dimension.
+//
+// The computation is the one of "RFC: MsModeling 支持 Decode Context Parallel 仿真"
+// 2.1.4.1-2.1.4.4 and "vllm-ascend PR #18870 解读" 4.3 / 4.5: for every query token,
+// softmax(scale * q K^T) V over the latent rows its top-k list selects, with the
+// per-head log-sum-exp, optionally restricted to one sequence shard (DCP).
+//
+// Why one CTA suffices at 64 heads.  The output O^T[v, heads] (512 output columns as
+// four 128-lane blocks, the heads as columns) takes 4 x 64 = 256 TMEM columns.  q's
+// latent part would take another 256 if its 64 heads sat in 128 lanes the usual way
+// (one head per lane, 512 values = 256 bf16 pairs), leaving nothing for the scores.
+// Here the latent columns are split in two halves and the halves are stacked in M:
+//   * TMEM lanes 0-63 hold heads 0-63 with latent columns [0, 256), lanes 64-127 the
+//     same heads with columns [256, 512): 128 TMEM columns for all of q's latent part;
+//   * each latent step of QK^T is one M=128, N=64 MMA whose B operand is the tile's 32
+//     rows in column block j followed by the same rows in block j+4 (the gathered
+//     blocks are laid out in that order, so the 64 operand rows are contiguous);
+//   * of the 128 x 64 result, lanes 0-63 x columns 0-31 are the partial scores over
+//     the first half (head, row), lanes 64-127 x columns 32-63 those over the second
+//     half; the two other quarters pair a head with the other half of a row and are
+//     never read.  The rope columns (64) add into the first quarter with four M=128,
+//     N=32 MMAs whose A operand is q's rope part in shared memory (rows 64-127 of that
+//     operand are whatever follows it in shared memory: they only feed unread lanes);
+//   * the softmax warps owning a head in the two halves (warps w and w+2, w = 0, 1)
+//     each take 16 of the tile's 32 rows, receive the other half's partials of those
+//     rows from their partner through shared memory, and keep one online softmax per
+//     head in step (both see the same maxima);
+//   * P.V is formed transposed, O^T[v, heads] += V^T[v, rows] P^T[rows, heads]: V^T is
+//     read straight from the gathered tile (MN-major), P^T from a shared-memory tile
+//     the softmax writes (K-major).
+// TMEM: q latent (128 columns), two score buffers (2 x 64), O^T (256).  With q out of
+// shared memory, five 36 KB stages of whole rows fit, enough to keep a gather stream
+// in flight without a second CTA.
+//
+// When a batch has fewer units (token, shard) than half the SMs, a cluster of G = 2
+// or 4 CTAs shares each unit: CTA c takes tiles c, c + G, ... with its own online
+// softmax, and the CTAs merge (O, m, l) over distributed shared memory at the end.
+//
+// Warp roles (320 threads): warps 0-3 softmax, O rescale and output (warp w owns TMEM
+// lane quadrant w: heads 32(w&1)..+31 of column half w>>1 for the scores, output
+// columns 128m + 32w + lane of block m for O^T); warps 4-7 gathers (TMA tile::gather4,
+// four rows per instruction); warp 8 issues QK^T; warp 9 issues P.V.  Every wait is
+// bounded; a wait that gives up records SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds
+// without trapping.
+#include <atomic>
+#include <cuda.h>
+#include <string.h>
+
+#include "sfa_internal.h"
+#include "sfa_ptx.cuh"
+#include "sfa_resolve.cuh"
+
+namespace sfa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kNt = 32;              // selected rows per tile
+constexpr int kStages = 5;           // gather pipeline depth
+constexpr int kThreads = 320;
+constexpr int kWarps = kThreads / 32;
+constexpr int kProducerWarp = 4;     // warps 4..7 issue the gathers
+constexpr int kProducerWarps = 4;
+constexpr int kQkWarp = 8;
+constexpr int kPvWarp = 9;
+constexpr int kNH = 64;              // padded heads: N of P.V, columns of O^T per block
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: P entries stay below 2^8
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kBlk = kNt * 128;                   // one 64-column SW128 block of a tile (4 KB)
+constexpr int kColBlocks = 9;                     // 8 latent blocks + the rope block
+constexpr int kStageBytes = kColBlocks * kBlk;    // 36 KB: whole rows
+// Offset of column block j in a stage: latent blocks j and j+4 side by side (so block j's
+// rows followed by block j+4's rows form one 64-row operand), the rope block last.
+__host__ __device__ constexpr int blk_off(int j) {
+  return j == 8 ? 8 * kBlk : (j < 4 ? 2 * j * kBlk : (2 * (j - 4) + 1) * kBlk);
+}
+constexpr int kOffQRope = kStages * kStageBytes;  // q rope [64 heads x 64] bf16, SW128
+constexpr int kQRopeBytes = kNH * 128;
+constexpr int kOffList = kOffQRope + kQRopeBytes; // also rows 64-127 of the rope A operand
+constexpr int kListCap = 64 * kNt;                // resolved rows kept at once (whole tiles)
+constexpr int kOffP = kOffList + kListCap * 4;
+constexpr int kPBytes = kNH * 128;                // P^T [64 heads x 32 rows] bf16, K-major SW128 rows
+constexpr int kOffX = kOffP + 2 * kPBytes;        // partner exchange: [4 warps][32 lanes][16] fp32
+constexpr int kXWarpFloats = 32 * 16;
+constexpr int kOffMisc = kOffX + 4 * kXWarpFloats * 4;
+// misc: per-head (m, l) [64] float2 (+0), rescale factors [64] (+512), the warps' partial
+// maxima [2 tile parities][4 warps][32] (+768), output scales [64] (+1792), the warps'
+// partial sums [4][32] (+2048), flags (+2560: [1] abort, [2] stop, [4..7] rescale per
+// warp), the TMEM address (+2624), per-warp counts (+2640)
+constexpr int kMiscBytes = 2640 + 4 * kWarps;
+constexpr int kOffBar = (kOffMisc + kMiscBytes + 7) / 8 * 8;
+constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQLoad = kBarKvEmpty + kStages,
+              kBarQReady = kBarQLoad + 1, kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2,
+              kBarPReady = kBarSFree + 2, kBarPFree = kBarPReady + 2, kBarPvFinal = kBarPFree + 2,
+              kBarMmaFin = kBarPvFinal + 1, kBarMmaFin2 = kBarMmaFin + 1, kBarNever = kBarMmaFin2 + 1,
+              kNumBars = kBarNever + 1;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kBlk % 1024 == 0, "SW128 operands: 1024-byte alignment");
+static_assert(kListCap * 4 >= kQRopeBytes, "rows 64-127 of the rope operand stay inside shared memory");
+static_assert(kListCap % kNt == 0, "list segments hold whole tiles");
+// the merge receives every CTA's scaled O^T for 4 blocks x 128 columns in the idle stages
+static_assert(4 * 128 * kNH * 4 <= kStages * kStageBytes, "merge buffer fits in the stages");
+
+constexpr long long kDrainLimit = 1LL << 40;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;   // q latent (128), S x 2 (128), O^T (4 x 64)
+
+struct StackParams {
+  DecodeParams p;
+  int num_rows;   // num_blocks * block_size (an out-of-range row used for padding)
+};
+
+// kInterleaved: shard layout.
+template <bool kInterleaved>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_stack_kernel(const __grid_constant__ CUtensorMap tmap_rows, const __grid_constant__ CUtensorMap tmap_qrope,
+                        const StackParams sp) {
+  const DecodeParams& p = sp.p;
+  extern __shared__ char smem_raw[];
+  char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  int* list_s = reinterpret_cast<int*>(smem + kOffList);
+  float* x_s = reinterpret_cast<float*>(smem + kOffX);
+  float2* ml_s = reinterpret_cast<float2*>(smem + kOffMisc);                   // [64] (m, l)
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffMisc + 512);           // [64]
+  float* mxs_base = reinterpret_cast<float*>(smem + kOffMisc + 768);          // [2][4][32]
+  float* scale_s = reinterpret_cast<float*>(smem + kOffMisc + 1792);          // [64]
+  float* lpart_s = reinterpret_cast<float*>(smem + kOffMisc + 2048);          // [4][32]
+  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 2560);
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + 2624);
+  int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 2640);             // [kWarps]
+  volatile int* abort_s = flags_s + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  uint32_t G;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(G));
+  const int unit = blockIdx.x / G;
+  const int T = p.B * p.Q;
+  // units go out last shard first (the heaviest shards of a sparse selection start first)
+  const int t = unit % T, r = p.n_splits - 1 - unit / T;
+  const int b = t / p.Q, qi = t % p.Q;
+  const int seq_len = p.seq_lens[b];
+  const int L = seq_len - (p.Q - 1 - qi);
+  const ShardSel sel = shard_sel(seq_len, L, r, p.n_splits, p.interleave);
+  const int bt_row = p.bt_per_token ? t : b;
+  const int32_t* idx = p.topk_idx + (size_t)t * p.top_k;
+  const long long wl = p.wait_limit;
+
+  // ---- set-up ----------------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarKvFull + s], kProducerWarps);
+      mbar_init(&bars[kBarKvEmpty + s], 1);
+    }
+    mbar_init(&bars[kBarQLoad], 1);
+    mbar_init(&bars[kBarQReady], 4);        // one arrival per warp 0-3 (each holds a quarter of q)
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[kBarSFull + x], 1);   // QK^T of the tile in this score buffer done
+      mbar_init(&bars[kBarSFree + x], 4);   // the four softmax warps read this score buffer
+      mbar_init(&bars[kBarPReady + x], 4);  // P in this buffer and O rescaled (one arrival per warp 0-3)
+      mbar_init(&bars[kBarPFree + x], 1);   // P.V has read this buffer's P (and updated O)
+    }
+    mbar_init(&bars[kBarPvFinal], 1);
+    mbar_init(&bars[kBarMmaFin], 1);
+    mbar_init(&bars[kBarMmaFin2], 1);
+    mbar_init(&bars[kBarNever], 1);         // nothing arrives: the stall test hook waits on it
+    for (int k = 0; k < 8; ++k) flags_s[k] = 0;
+    fence_barrier_init();
+    // q's rope columns of this token (rows 0..h-1) as the shared-memory A operand of the
+    // rope steps
+    mbar_arrive_expect_tx(&bars[kBarQLoad], (uint32_t)(p.h * 128));
+    tma_load_3d(smem_u32(smem + kOffQRope), &tmap_qrope, 512, 0, t, &bars[kBarQLoad]);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_base_s, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmap_rows);
+
+  // ---- index resolution: count per warp chunk, then ordered compaction into smem ----
+  const int chunk = ((p.top_k + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int c_begin = min(warp * chunk, p.top_k), c_end = min(c_begin + chunk, p.top_k);
+  const bool one_round = chunk <= 8 * 32;
+  int row_r[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) row_r[k] = -1;
+  {
+    int cnt = resolve_chunk<kInterleaved>(p, idx, c_begin, c_end, lane, sel, bt_row, crank == 0, row_r);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (lane == 0) wcount_s[warp] = cnt;
+  }
+  __syncthreads();
+  int total = 0, off = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = wcount_s[w];
+    if (w < warp) off += c;
+    total += c;
+  }
+  if (one_round) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const unsigned mask = __ballot_sync(0xffffffffu, row_r[k] >= 0);
+      const int o = off + __popc(mask & lanemask_lt());
+      if (row_r[k] >= 0 && o < kListCap) list_s[o] = row_r[k];
+      off += __popc(mask);
+    }
+  } else {
+    for (int j0 = c_begin; j0 < c_end && off < kListCap; j0 += 32) {
+      const int j = j0 + lane;
+      const int row = j < c_end ? resolve_row<kInterleaved>(p, bt_row, __ldg(idx + j), sel, false) : -1;
+      const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+      const int o = off + __popc(mask & lanemask_lt());
+      if (row >= 0 && o < kListCap) list_s[o] = row;
+      off += __popc(mask);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  const int n_tiles = (total + kNt - 1) / kNt;                              // tiles of the unit
+  const int n_local = n_tiles > (int)crank ? (n_tiles - (int)crank + (int)G - 1) / (int)G : 0;   // this CTA's
+
+  auto fail = [&](void) {
+    report_status(p.status, kStatusTimeout);
+    *abort_s = 1;
+  };
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, wl));
+  };
+
+  // warps 0-3: running max of head `head` (log2 units; the same in the two warps of a
+  // head) and this warp's share of its running sum (the two shares are added at the end)
+  float m_ref = -INFINITY, l_part = 0.f;
+  const int hg = warp & 1;          // head group: heads 32 hg .. 32 hg + 31
+  const int half = (warp >> 1) & 1; // latent column half of this warp's TMEM quadrant
+  const int head = 32 * hg + lane;
+  if (warp < 4) {
+    // =================== softmax and O rescale (warps 0-3) ==========================
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    {
+      // q's latent columns [256 half, 256 half + 256) of head `head` into this warp's
+      // quadrant as bf16 pairs (the A operand of the latent steps); heads past h are zeros
+      const bool have = head < p.h;
+      const uint4* qsrc =
+          reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.h + (have ? head : 0)) * kDQK + 256 * half);
+#pragma unroll 1
+      for (int c64 = 0; c64 < 2; ++c64) {   // 64 TMEM columns (128 latent values) per round
+        uint4 x[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) x[k] = have ? __ldg(qsrc + 16 * c64 + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t v[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[4 * k] = x[4 * u + k].x; v[4 * k + 1] = x[4 * u + k].y;
+            v[4 * k + 2] = x[4 * u + k].z; v[4 * k + 3] = x[4 * u + k].w;
+          }
+          tmem_st16(lane_base + kColQ + 64 * c64 + 16 * u, v);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarQReady]);
+    }
+    const float c_scale = p.scale * kLog2e;
+    // |scale| in log2 units, at least 1e-30: masked scores are -inf, and -inf times a zero
+    // scale would be NaN.  For a zero scale every valid weight still rounds to exactly 1
+    // (|scores * 1e-30| is far below one ulp of 1), the uniform average the definition gives.
+    const float c_abs = fmaxf(fabsf(c_scale), 1e-30f);
+    const int partner = warp ^ 2;
+    const int row0 = 16 * half;         // this warp finishes tile rows row0 .. row0 + 15
+    // 16-byte slot q4 of this lane's 64-byte exchange row, rotated so a quarter warp's
+    // accesses fall in distinct banks
+    const int xrot = (lane >> 1) & 3;
+    // Warps 0-3 leave the tile loop together: warp 0 alone reads the abort flag at the top
+    // of each tile and publishes the decision before the barrier the others wait at.
+    for (int i = 0; i < n_local; ++i) {
+      const int bb = i & 1;
+      if (warp == 0) {
+        bool go = !*abort_s;
+        if (go && !wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); go = false; }
+        // P buffer bb is free once P.V of tile i-2 has read it
+        if (go && i >= 2 && !wait_warp(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); go = false; }
+        if (lane == 0) flags_s[2] = go ? 0 : 1;
+      }
+      named_barrier(1, 128);   // A: the scores of tile i are in TMEM and P buffer bb is free
+      if (flags_s[2]) break;
+      tc_fence_after();
+      // this quadrant's partial scores of the tile: lanes of heads 32 hg.., the 32 columns
+      // of its column half (first half: columns 0-31, second half: columns 32-63)
+      uint32_t v[32];
+      tmem_ld32(lane_base + kColS + 64 * bb + 32 * half, v);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarSFree + bb]);
+      {
+        // the partner finishes the other 16 rows: send it this half's partials of them
+        const int snd = half ? 0 : 16;
+        float* dst = x_s + warp * kXWarpFloats + lane * 16;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          *reinterpret_cast<uint4*>(dst + 4 * (q4 ^ xrot)) =
+              make_uint4(v[snd + 4 * q4], v[snd + 4 * q4 + 1], v[snd + 4 * q4 + 2], v[snd + 4 * q4 + 3]);
+      }
+      named_barrier(4 + hg, 64);   // X: the two halves' partials of this head group are published
+      float s[16];
+      {
+        const float* src = x_s + partner * kXWarpFloats + lane * 16;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 y = *reinterpret_cast<const uint4*>(src + 4 * (q4 ^ xrot));
+          s[4 * q4] = __uint_as_float(v[row0 + 4 * q4]) + __uint_as_float(y.x);
+          s[4 * q4 + 1] = __uint_as_float(v[row0 + 4 * q4 + 1]) + __uint_as_float(y.y);
+          s[4 * q4 + 2] = __uint_as_float(v[row0 + 4 * q4 + 2]) + __uint_as_float(y.z);
+          s[4 * q4 + 3] = __uint_as_float(v[row0 + 4 * q4 + 3]) + __uint_as_float(y.w);
+        }
+      }
+      const int g = (int)crank + (int)G * i;   // the unit's tile index
+      const int nvalid = min(kNt, total - kNt * g);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float x = s[j];
+        if (c_scale < 0.f) x = -x;   // keep max(s) * |c| == max(s * c) for a negative scale
+        s[j] = (row0 + j >= nvalid || head >= p.h) ? -INFINITY : x;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int j = 1; j < 16; ++j) mx = fmaxf(mx, s[j]);
+      float* mx_s = mxs_base + 128 * bb;   // [4 warps][32 heads] of this tile parity
+      mx_s[warp * 32 + lane] = mx;
+      named_barrier(2, 128);   // B: every warp's partial max of tile i is published
+      // the same maximum in both warps of a head: fmaxf is exact and symmetric
+      const float mt = fmaxf(mx_s[hg * 32 + lane], mx_s[(hg + 2) * 32 + lane]) * c_abs;
+      float m_new = m_ref;
+      if (head < p.h && (i == 0 || mt > m_ref + kRescaleThreshold)) m_new = fmaxf(mt, m_ref);
+      const float alpha = (i == 0 || head >= p.h) ? 1.f : ex2(m_ref - m_new);
+      m_ref = m_new;
+      uint32_t pk[8];
+      float sm = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e0 = head < p.h ? ex2(fmaf(s[2 * j], c_abs, -m_new)) : 0.f;
+        const float e1 = head < p.h ? ex2(fmaf(s[2 * j + 1], c_abs, -m_new)) : 0.f;
+        sm += e0 + e1;
+        pk[j] = pack_bf16(e0, e1);
+      }
+      l_part = l_part * alpha + sm;
+      {
+        // this head's row of P^T, tile rows row0..row0+15 = 16-byte chunks 2 half and
+        // 2 half + 1 of the K-major SW128 row
+        char* p_row = smem + kOffP + bb * kPBytes + head * 128;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          *reinterpret_cast<uint4*>(p_row + (((2 * half + u) ^ (head & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        fence_proxy_async_smem();
+      }
+      // O is rescaled (rarely: the reference max moves only by more than the threshold)
+      // once P.V of the previous tile has completed.  A warp that rescales one of its
+      // heads waits for that itself; the barrier below passes the ordering to the others.
+      // (Tile i+1 waits on the same phase of that buffer again: it cannot have moved on,
+      // P.V of tile i+1 is not issued yet.)
+      const bool resc_w = __any_sync(0xffffffffu, alpha != 1.f);
+      if (resc_w && i >= 1 && !wait_warp(&bars[kBarPFree + (bb ^ 1)], ((i - 1) >> 1) & 1)) fail();
+      if (half == 0) alpha_s[head] = alpha;
+      if (lane == 0) flags_s[4 + warp] = resc_w ? 1 : 0;
+      named_barrier(3, 128);   // C: whether O is rescaled, and by what
+      if ((flags_s[4] | flags_s[5] | flags_s[6] | flags_s[7]) && !*abort_s) {
+        tc_fence_after();
+        // O^T lane v holds output column v of every head: scale column hh by alpha[hh]
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+          for (int c16 = 0; c16 < kNH / 16; ++c16) {
+            uint32_t o[16];
+            tmem_ld16(lane_base + kColO + kNH * m + 16 * c16, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[16 * c16 + k]);
+            tmem_st16(lane_base + kColO + kNH * m + 16 * c16, o);
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarPReady + bb]);
+    }
+  } else if (warp < kProducerWarp + kProducerWarps) {
+    // =================== gathers ===================================================
+    // Producer warp pw issues the gathers of row groups g = pw, pw + 4 of each of its
+    // tiles (4 rows each, all nine 64-column blocks): 18 per tile, one per lane.
+    const int pw = warp - kProducerWarp;
+    int seg = 0;
+    int n = 0;
+    bool ok = true;
+    for (; n < n_local && !*abort_s; ++n) {
+      const int s = n % kStages;
+      if (n >= kStages && !(ok = wait_warp(&bars[kBarKvEmpty + s], ((n / kStages) - 1) & 1))) break;
+      const int first = kNt * ((int)crank + (int)G * n);
+      if (first >= (seg + 1) * kListCap) {
+        // rare (more valid entries than the list holds): this warp re-resolves the
+        // entries of its own row groups for the segment that holds this tile
+        seg = first / kListCap;
+        int ord = 0;
+        for (int j0 = 0; j0 < p.top_k; j0 += 32) {
+          const int j = j0 + lane;
+          const int row = j < p.top_k ? resolve_row<kInterleaved>(p, bt_row, __ldg(idx + j), sel, false) : -1;
+          const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+          const int o = ord + __popc(mask & lanemask_lt()) - seg * kListCap;
+          if (row >= 0 && o >= 0 && o < kListCap && ((o % kNt) / 4) % kProducerWarps == pw) list_s[o] = row;
+          ord += __popc(mask);
+        }
+        __syncwarp();
+      }
+      char* st = smem + s * kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarKvFull + s], kStageBytes / kProducerWarps);
+      __syncwarp();
+      constexpr int kGroupsPerWarp = kNt / 4 / kProducerWarps;   // 2
+      if (lane < kColBlocks * kGroupsPerWarp) {
+        const int g = pw + kProducerWarps * (lane / kColBlocks), j = lane % kColBlocks;
+        int rr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int e = first + 4 * g + k;
+          rr[k] = e < total ? list_s[e - seg * kListCap] : sp.num_rows;   // past the end: zero fill
+        }
+        tma_gather4(smem_u32(st + blk_off(j) + g * 512), &tmap_rows, 64 * j, rr[0], rr[1], rr[2], rr[3],
+                    &bars[kBarKvFull + s]);
+      }
+      __syncwarp();
+    }
+    if (!ok) fail();
+    // no gather of this CTA may still be landing in shared memory at exit
+    for (int k = n > kStages ? n - kStages : 0; k < n; ++k)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarKvFull + k % kStages], (k / kStages) & 1, kDrainLimit)))
+        report_status(p.status, kStatusTimeout);
+  } else if (warp == kQkWarp || warp == kPvWarp) {
+    // =================== tcgen05 MMA issue: QK^T (warp 8) and P.V (warp 9) ========
+    // q's rope load must have landed before the CTA exits, whatever happens below
+    bool q_landed = false;
+    if (lane == 0 && n_local > 0) {
+      bool ok = true;
+      if (warp == kQkWarp) {
+        // test hook: a wait that cannot complete, so the wait limit runs out
+        ok = !p.stall || mbar_wait(&bars[kBarNever], 0, wl);
+        ok = ok && (q_landed = mbar_wait(&bars[kBarQLoad], 0, wl)) && mbar_wait(&bars[kBarQReady], 0, wl);
+        tc_fence_after();
+        // latent steps: M = 128 (two column halves of 64 heads), N = 64 (block j's rows,
+        // then block j+4's); rope steps: M = 128 (q rope rows first), N = 32
+        const uint32_t id_lat = idesc_bf16(128, 2 * kNt, 0, 0);
+        const uint32_t id_rope = idesc_bf16(128, kNt, 0, 0);
+        const uint32_t qrope = smem_u32(smem + kOffQRope);
+        for (int n = 0; ok && n < n_local && !*abort_s; ++n) {
+          const int s = n % kStages, bb = n & 1;
+          if (!(ok = mbar_wait(&bars[kBarKvFull + s], (n / kStages) & 1, wl))) break;
+          // the score buffer is free once the softmax has read tile n-2 from it
+          if (n >= 2 && !(ok = mbar_wait(&bars[kBarSFree + bb], ((n >> 1) - 1) & 1, wl))) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * kStageBytes);
+          const uint32_t d = tmem + kColS + 64 * bb;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            mma_ts(d, tmem + kColQ + 8 * k,
+                   smem_desc(st + blk_off(k >> 2) + (k & 3) * 32, 16, 1024, kSwizzle128), id_lat, k > 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(d, smem_desc(qrope + 32 * k, 16, 1024, kSwizzle128),
+                   smem_desc(st + blk_off(8) + 32 * k, 16, 1024, kSwizzle128), id_rope, 1);
+          mma_commit(&bars[kBarSFull + bb]);
+        }
+      } else {
+        // A = V^T: output columns 128m..128m+127 (latent blocks 2m, 2m+1, 8 KB apart in
+        // the stage) of 16 tile rows, MN-major; B = P^T: 64 heads x 16 rows, K-major
+        const uint32_t id_pv = idesc_bf16(128, kNH, 1, 0);
+        const uint32_t pt = smem_u32(smem + kOffP);
+        static_assert(blk_off(1) - blk_off(0) == 2 * kBlk && blk_off(3) - blk_off(2) == 2 * kBlk &&
+                          blk_off(5) - blk_off(4) == 2 * kBlk && blk_off(7) - blk_off(6) == 2 * kBlk,
+                      "the two blocks of an output block sit 2 kBlk apart");
+        for (int n = 0; ok && n < n_local && !*abort_s; ++n) {
+          const int s = n % kStages, bb = n & 1;
+          if (!(ok = mbar_wait(&bars[kBarPReady + bb], (n >> 1) & 1, wl))) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * kStageBytes);
+          const uint32_t ptb = pt + bb * kPBytes;
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int k = 0; k < kNt / 16; ++k)
+              mma_ss(tmem + kColO + kNH * m,
+                     smem_desc(st + blk_off(2 * m) + 2048 * k, 2 * kBlk, 1024, kSwizzle128),
+                     smem_desc(ptb + 32 * k, 16, 1024, kSwizzle128), id_pv, (n > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars[kBarKvEmpty + s]);
+          mma_commit(&bars[kBarPFree + bb]);
+          if (n == n_local - 1) mma_commit(&bars[kBarPvFinal]);
+        }
+      }
+      if (!ok) fail();
+      // every MMA this thread issued has completed before TMEM is released
+      uint64_t* fin_bar = &bars[warp == kQkWarp ? kBarMmaFin : kBarMmaFin2];
+      mma_commit(fin_bar);
+      if (!mbar_wait(fin_bar, 0, kDrainLimit)) report_status(p.status, kStatusTimeout);
+    }
+    if (warp == kQkWarp && lane == 0 && !q_landed && !mbar_wait(&bars[kBarQLoad], 0, kDrainLimit))
+      report_status(p.status, kStatusTimeout);
+  }
+
+  // ---- merge of the cluster's partial results and the output ---------------------
+  // Every thread of every CTA of the cluster reaches both cluster barriers.
+  __syncwarp();
+  bool have_o = false;
+  if (warp < 4) {
+    if (n_local > 0 && !*abort_s) {
+      have_o = wait_warp(&bars[kBarPvFinal], 0);
+      if (!have_o) fail();
+    }
+    lpart_s[warp * 32 + lane] = l_part;
+    named_barrier(2, 128);
+    if (warp < 2) {
+      // head 32 warp + lane: its sum is the two column-half warps' shares
+      const float l_sum = lpart_s[warp * 32 + lane] + lpart_s[(warp + 2) * 32 + lane];
+      ml_s[head] = (have_o && head < p.h) ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
+    }
+  }
+  tc_fence_before();
+  cluster_sync();   // every CTA's (m, l) is published
+  tc_fence_after();
+  if (warp < 2) {
+    // head `head`: the merged max M, total sum L and this CTA's weight exp2(m - M) / L
+    float M = -INFINITY;
+    for (uint32_t c = 0; c < G; ++c) {
+      float mc;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(mc) : "r"(mapa(&ml_s[head], c) + 0u));
+      M = fmaxf(M, mc);
+    }
+    float Lsum = 0.f;
+    for (uint32_t c = 0; c < G; ++c) {
+      float mc, lc;
+      const uint32_t a = mapa(&ml_s[head], c);
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(mc) : "r"(a));
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(lc) : "r"(a + 4u));
+      if (mc != -INFINITY) Lsum += ex2(mc - M) * lc;
+    }
+    const float mine = ml_s[head].x;
+    scale_s[head] = (Lsum > 0.f && mine != -INFINITY) ? ex2(mine - M) / Lsum : 0.f;
+    if (crank == 0 && head < p.h && !*abort_s)
+      p.lse[((size_t)r * T + t) * p.h + head] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
+  }
+  float* outp = p.out + ((size_t)r * T + t) * p.h * kDV;
+  const int v = warp * 32 + lane;   // TMEM lane of warps 0-3: output column v of each 128-column block
+  // the merge buffer (in the idle stages): for block m, owner m % G, slot of source CTA c:
+  //   recv[((c * (4 / G) + m / G) * 128 + v) * 64 + hh], 16-byte chunks swizzled by v
+  float* recv = reinterpret_cast<float*>(smem);
+  const int blocks_per = 4 / (int)G;
+  if (warp < 4) {
+    named_barrier(2, 128);
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      uint32_t o[kNH];
+      if (have_o) {
+#pragma unroll
+        for (int c16 = 0; c16 < kNH / 16; ++c16)
+          tmem_ld16(lane_base + kColO + kNH * m + 16 * c16, *reinterpret_cast<uint32_t(*)[16]>(&o[16 * c16]));
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int k = 0; k < kNH; ++k) o[k] = 0u;
+      }
+      if (G == 1) {
+        // the whole output is this CTA's: one coalesced 128-byte row segment per (head, warp)
+        if (!*abort_s) {
+#pragma unroll
+          for (int hh = 0; hh < kNH; ++hh)
+            if (hh < p.h) outp[(size_t)hh * kDV + 128 * m + v] = __uint_as_float(o[hh]) * scale_s[hh];
+        }
+        continue;
+      }
+      const uint32_t owner = (uint32_t)m % G;
+      float* slot = recv + ((size_t)(crank * blocks_per + m / (int)G) * 128 + v) * kNH;
+      const uint32_t dst = mapa(slot, owner);
+#pragma unroll
+      for (int c4 = 0; c4 < kNH / 4; ++c4) {
+        const int sw = c4 ^ (v & (kNH / 4 - 1));
+        st_cluster_v4(dst + 16u * sw, __float_as_uint(__uint_as_float(o[4 * c4]) * scale_s[4 * c4]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 1]) * scale_s[4 * c4 + 1]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 2]) * scale_s[4 * c4 + 2]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 3]) * scale_s[4 * c4 + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  cluster_sync();   // every CTA's scaled partial O has landed with its owner
+  tc_fence_after();
+  if (G > 1 && warp < 4 && !*abort_s) {
+    // this CTA's output blocks: the sum of the G scaled partials
+    for (int m = (int)crank; m < 4; m += (int)G) {
+      float acc[kNH];
+#pragma unroll
+      for (int k = 0; k < kNH; ++k) acc[k] = 0.f;
+      for (uint32_t c = 0; c < G; ++c) {
+        const float* slot = recv + ((size_t)(c * blocks_per + m / (int)G) * 128 + v) * kNH;
+#pragma unroll
+        for (int c4 = 0; c4 < kNH / 4; ++c4) {
+          const float4 x = *reinterpret_cast<const float4*>(slot + 4 * (c4 ^ (v & (kNH / 4 - 1))));
+          acc[4 * c4] += x.x; acc[4 * c4 + 1] += x.y; acc[4 * c4 + 2] += x.z; acc[4 * c4 + 3] += x.w;
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < kNH; ++hh)
+        if (hh < p.h) outp[(size_t)hh * kDV + 128 * m + v] = acc[hh];
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------------
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <bool kIL>
+constexpr auto stack_kernel() {
+  return decode_stack_kernel<kIL>;
+}
+
+}  // namespace
+
+bool stack_supports(int h) { return h > 32 && h <= kNH; }
+
+cudaError_t prepare_decode_stack() {
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
+    for (auto kernel : {stack_kernel<false>(), stack_kernel<true>()}) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
+    attr_set[dev].store(true, std::memory_order_release);
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_stack(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
+                                int n_sms, cudaStream_t stream) {
+  const long long T = (long long)p.B * p.Q;
+  const long long units = T * p.n_splits;
+  if (units == 0) return cudaSuccess;
+  const long long num_rows = (long long)p.num_blocks * p.block_size;
+  cudaError_t e = prepare_decode_stack();
+  if (e != cudaSuccess) return e;
+  const int G = narrow_cluster_size(units, n_sms);
+  if (!stack_supports(p.h) || num_rows >= 0x7fffffffLL || units * G > 0x7fffffffLL) return cudaErrorInvalidValue;
+  StackParams sp;
+  sp.p = p;
+  sp.num_rows = (int)num_rows;
+  const bool il = p.interleave > 0 && p.n_splits > 1;
+  auto kernel = il ? stack_kernel<true>() : stack_kernel<false>();
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)(units * G), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)G;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, rows_map, qrope_map, sp);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace sfa

@@ -765,19 +765,21 @@ cudaError_t prepare_decode_tc() {
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, bool small_heads, cudaStream_t stream) {
+cudaError_t launch_decode_tc(const DecodeParams& p, int kernel_id, cudaStream_t stream) {
   const long long T = (long long)p.B * p.Q;
   const long long units = T * p.n_splits;
   if (units == 0) return cudaSuccess;
   const long long num_rows = (long long)p.num_blocks * p.block_size;
   if (num_rows >= 0x7fffffffLL || 2 * units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (small_heads) {
+  if (kernel_id == 2 || kernel_id == 3) {
     // whole rows as nine 64-column SW128 boxes from one map; q's rope columns as one box
     CUtensorMap rows, qrope;
-    if (!narrow_supports(p.h) || !make_row_map(&rows, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    const bool ok_h = kernel_id == 2 ? narrow_supports(p.h) : stack_supports(p.h);
+    if (!ok_h || !make_row_map(&rows, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_q_map(&qrope, p.q, p.h, T, p.h, 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    return launch_decode_narrow(p, rows, qrope, stream);
+    return kernel_id == 2 ? launch_decode_narrow(p, rows, qrope, stream)
+                          : launch_decode_stack(p, rows, qrope, device_sm_count(), stream);
   }
   TcParams tp;
   tp.p = p;

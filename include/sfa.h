@@ -329,7 +329,8 @@ sfa_status sfa_decode_noalloc(const void *q, const void *kv, const int32_t *bloc
  * sfa_decode_launches -- how many kernels one sfa_decode call with these
  * arguments enqueues (merge != 0: out/lse given with n_splits > 1), and through
  * *tensor_core_path which kernel serves it: 2 = the small-head tcgen05 kernel
- * (h <= 32), 1 = the CTA-pair tcgen05 kernel, 0 = the CUDA-core kernel.
+ * (h <= 32), 3 = the stacked-half tcgen05 kernel (33 <= h <= 64), 1 = the CTA-pair
+ * tcgen05 kernel, 0 = the CUDA-core kernel.
  * tensor_core_path may be NULL.  Returns -1 for invalid arguments.
  */
 int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_splits, int merge,
@@ -338,7 +339,8 @@ int sfa_decode_launches(int B, int Q, int h, int top_k, int block_size, int n_sp
 /*
  * sfa_set_kernel_path -- kernel family for sfa_decode calls made afterwards in
  * this process: 0 = automatic (the small-head tcgen05 kernel for h <= 32, the
- * CTA-pair tcgen05 kernel above), 1 = the CUDA-core kernel for every shape, 2 = the
+ * stacked-half tcgen05 kernel for 33 <= h <= 64, the CTA-pair tcgen05 kernel
+ * above), 1 = the CUDA-core kernel for every shape, 2 = the
  * CTA-pair tcgen05 kernel for every shape.  Paths 1 and 2 exist to cross-check the
  * kernels against each other.  Returns the previous setting, or -1 (and changes
  * nothing) for another value.

@@ -166,11 +166,11 @@ def forced_path(request):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_decode_random_shapes_forced_paths(seed, forced_path):
-    """The same random shapes on the CUDA-core kernel and, for h <= 32, on the CTA-pair
-    kernel (which the automatic choice gives only to h > 32)."""
+    """The same random shapes on the CUDA-core kernel and, for h <= 64, on the CTA-pair
+    kernel (which the automatic choice gives only to h > 64)."""
     w, g, rng = _decode_case(seed)
-    if forced_path == 2 and w.h > 32:
-        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 32")
+    if forced_path == 2 and w.h > 64:
+        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 64")
     inp = workloads.make(w, device="cuda")
     inp.topk_idx = _salt_indices(inp, rng)
     ref_out, ref_lse = oracle.decode(problem_of(inp))

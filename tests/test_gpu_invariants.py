@@ -21,12 +21,14 @@ pytestmark = pytest.mark.gpu
 W = workloads.Workload
 CASE_WIDE = W("inv", B=3, Q=2, h=128, S=5000, S_min=300, top_k=700, n_splits=1, index_kind="causal", seed=51)
 CASE_NARROW = W("inv_h16", B=3, Q=2, h=16, S=5000, S_min=300, top_k=700, n_splits=1, index_kind="causal", seed=52)
+CASE_MID = W("inv_h48", B=3, Q=2, h=48, S=5000, S_min=300, top_k=700, n_splits=1, index_kind="causal", seed=53)
 
 
 # (kernel path, case): the tcgen05 kernels (automatic: CTA pair at h=128, small-head at
-# h=16; forced CTA pair at h=16) and the CUDA-core kernel
-@pytest.fixture(params=[(0, CASE_WIDE), (1, CASE_WIDE), (0, CASE_NARROW), (2, CASE_NARROW), (1, CASE_NARROW)],
-                ids=["pair-h128", "cudacore-h128", "small-h16", "pair-h16", "cudacore-h16"])
+# h=16, stacked halves at h=48; forced CTA pair at h=16) and the CUDA-core kernel
+@pytest.fixture(params=[(0, CASE_WIDE), (1, CASE_WIDE), (0, CASE_NARROW), (2, CASE_NARROW), (1, CASE_NARROW),
+                        (0, CASE_MID)],
+                ids=["pair-h128", "cudacore-h128", "small-h16", "pair-h16", "cudacore-h16", "stack-h48"])
 def kernel_path(request):
     global CASE
     path, CASE = request.param

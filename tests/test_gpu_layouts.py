@@ -42,8 +42,9 @@ INTERLEAVED = [
 CASES = [(w, g) for w, gs in INTERLEAVED for g in gs]
 
 
-# 0 automatic (small-head kernel for h <= 32, CTA pair above), 1 CUDA-core, 2 CTA pair for
-# every h (run only where it differs from the automatic choice)
+# 0 automatic (small-head kernel for h <= 32, stacked-half kernel for h <= 64, CTA pair
+# above), 1 CUDA-core, 2 CTA pair for every h (run only where it differs from the automatic
+# choice)
 @pytest.fixture(params=[0, 1, 2], ids=["auto", "cudacore", "pair"])
 def kernel_path(request):
     prev = sfa.set_kernel_path(request.param)
@@ -52,8 +53,8 @@ def kernel_path(request):
 
 
 def _skip_duplicate(path, h):
-    if path == 2 and h > 32:
-        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 32")
+    if path == 2 and h > 64:
+        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 64")
 
 
 def _run(inp, bt, n, g, per_token, merge):

@@ -61,9 +61,10 @@ SMALL = [
 ]
 
 # which kernel decode_launches reports per kernel-path setting (0 automatic, 1 CUDA-core,
-# 2 CTA-pair tcgen05): 2 = small-head tcgen05, 1 = CTA-pair tcgen05, 0 = CUDA-core
+# 2 CTA-pair tcgen05): 2 = small-head tcgen05, 3 = stacked-half tcgen05, 1 = CTA-pair
+# tcgen05, 0 = CUDA-core
 def expected_kernel(path, h):
-    return {1: 0, 2: 1}.get(path, 2 if h <= 32 else 1)
+    return {1: 0, 2: 1}.get(path, 2 if h <= 32 else (3 if h <= 64 else 1))
 
 
 @pytest.fixture(params=[0, 1, 2], ids=["auto", "cudacore", "pair"])
@@ -75,8 +76,8 @@ def kernel_path(request):
 
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
 def test_small_cases_every_element(w, kernel_path):
-    if kernel_path == 2 and w.h > 32:
-        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 32")
+    if kernel_path == 2 and w.h > 64:
+        pytest.skip("the automatic path already runs the CTA-pair kernel for h > 64")
     assert sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1] == expected_kernel(kernel_path, w.h)
     inp = workloads.make(w, device="cuda")
     prob = problem_of(inp)
