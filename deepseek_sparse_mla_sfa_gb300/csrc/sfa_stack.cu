@@ -11,21 +11,20 @@
 // latent part would take another 256 if its 64 heads sat in 128 lanes the usual way
 // (one head per lane, 512 values = 256 bf16 pairs), leaving nothing for the scores.
 // Here the latent columns are split in two halves and the halves are stacked in M:
-//   * TMEM lanes 0-63 hold heads 0-63 with latent columns [0, 256), lanes 64-127 the
-//     same heads with columns [256, 512): 128 TMEM columns for all of q's latent part;
+//   * TMEM lane 32w + 16c + j holds head 16w + j with latent columns [256c, 256c + 256)
+//     (w = 0..3, c = 0, 1, j = 0..15): 128 TMEM columns for all of q's latent part, and
+//     each lane quadrant (the lanes one warp can read) holds 16 heads in both halves;
 //   * each latent step of QK^T is one M=128, N=64 MMA whose B operand is the tile's 32
 //     rows in column block j followed by the same rows in block j+4 (the gathered
 //     blocks are laid out in that order, so the 64 operand rows are contiguous);
-//   * of the 128 x 64 result, lanes 0-63 x columns 0-31 are the partial scores over
-//     the first half (head, row), lanes 64-127 x columns 32-63 those over the second
-//     half; the two other quarters pair a head with the other half of a row and are
-//     never read.  The rope columns (64) add into the first quarter with four M=128,
-//     N=32 MMAs whose A operand is q's rope part in shared memory (rows 64-127 of that
-//     operand are whatever follows it in shared memory: they only feed unread lanes);
-//   * the softmax warps owning a head in the two halves (warps w and w+2, w = 0, 1)
-//     each take 16 of the tile's 32 rows, receive the other half's partials of those
-//     rows from their partner through shared memory, and keep one online softmax per
-//     head in step (both see the same maxima);
+//   * a lane of half c reads its half's partial scores in columns 32c..32c+31 of the
+//     128 x 64 result (the other 32 columns pair the head with the other half of a row
+//     and are never read).  The rope columns (64) add into columns 0-31 with four M=128,
+//     N=32 MMAs whose A operand is q's rope part in shared memory, in the rows of the
+//     first-half lanes;
+//   * the two lanes of a head (16 apart in one warp) each finish 16 of the tile's 32 rows:
+//     one warp shuffle brings the other half's partials of those rows, another the
+//     other lane's maximum, so both keep the same online softmax of the head;
 //   * P.V is formed transposed, O^T[v, heads] += V^T[v, rows] P^T[rows, heads]: V^T is
 //     read straight from the gathered tile (MN-major), P^T from a shared-memory tile
 //     the softmax writes (K-major).
@@ -38,7 +37,7 @@
 // softmax, and the CTAs merge (O, m, l) over distributed shared memory at the end.
 //
 // Warp roles (320 threads): warps 0-3 softmax, O rescale and output (warp w owns TMEM
-// lane quadrant w: heads 32(w&1)..+31 of column half w>>1 for the scores, output
+// lane quadrant w: heads 16w..16w+15 in both column halves for the scores, output
 // columns 128m + 32w + lane of block m for O^T); warps 4-7 gathers (TMA tile::gather4,
 // four rows per instruction); warp 8 issues QK^T; warp 9 issues P.V.  Every wait is
 // bounded; a wait that gives up records SFA_ERR_DEVICE_TIMEOUT and the kernel unwinds
@@ -78,20 +77,17 @@ constexpr int kStageBytes = kColBlocks * kBlk;    // 36 KB: whole rows
 __host__ __device__ constexpr int blk_off(int j) {
   return j == 8 ? 8 * kBlk : (j < 4 ? 2 * j * kBlk : (2 * (j - 4) + 1) * kBlk);
 }
-constexpr int kOffQRope = kStages * kStageBytes;  // q rope [64 heads x 64] bf16, SW128
-constexpr int kQRopeBytes = kNH * 128;
-constexpr int kOffList = kOffQRope + kQRopeBytes; // also rows 64-127 of the rope A operand
+constexpr int kOffQRope = kStages * kStageBytes;  // q rope as a 128-row A operand, SW128
+constexpr int kQRopeBytes = 128 * 128;            // row 32w + j: head 16w + j (rows 32w+16.. unused)
+constexpr int kOffList = kOffQRope + kQRopeBytes;
 constexpr int kListCap = 64 * kNt;                // resolved rows kept at once (whole tiles)
 constexpr int kOffP = kOffList + kListCap * 4;
 constexpr int kPBytes = kNH * 128;                // P^T [64 heads x 32 rows] bf16, K-major SW128 rows
-constexpr int kOffX = kOffP + 2 * kPBytes;        // partner exchange: [4 warps][32 lanes][16] fp32
-constexpr int kXWarpFloats = 32 * 16;
-constexpr int kOffMisc = kOffX + 4 * kXWarpFloats * 4;
-// misc: per-head (m, l) [64] float2 (+0), rescale factors [64] (+512), the warps' partial
-// maxima [2 tile parities][4 warps][32] (+768), output scales [64] (+1792), the warps'
-// partial sums [4][32] (+2048), flags (+2560: [1] abort, [2] stop, [4..7] rescale per
-// warp), the TMEM address (+2624), per-warp counts (+2640)
-constexpr int kMiscBytes = 2640 + 4 * kWarps;
+constexpr int kOffMisc = kOffP + 2 * kPBytes;
+// misc: per-head (m, l) [64] float2 (+0), rescale factors [64] (+512), output scales [64]
+// (+768), flags (+1024: [1] abort), the warps' stop and rescale flags [2 tile parities]
+// [4 warps] (+1088, +1120), the TMEM address (+1152), per-warp counts (+1168)
+constexpr int kMiscBytes = 1168 + 4 * kWarps;
 constexpr int kOffBar = (kOffMisc + kMiscBytes + 7) / 8 * 8;
 constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQLoad = kBarKvEmpty + kStages,
               kBarQReady = kBarQLoad + 1, kBarSFull = kBarQReady + 1, kBarSFree = kBarSFull + 2,
@@ -101,7 +97,6 @@ constexpr int kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarQLoad = kB
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kBlk % 1024 == 0, "SW128 operands: 1024-byte alignment");
-static_assert(kListCap * 4 >= kQRopeBytes, "rows 64-127 of the rope operand stay inside shared memory");
 static_assert(kListCap % kNt == 0, "list segments hold whole tiles");
 // the merge receives every CTA's scaled O^T for 4 blocks x 128 columns in the idle stages
 static_assert(4 * 128 * kNH * 4 <= kStages * kStageBytes, "merge buffer fits in the stages");
@@ -125,15 +120,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   int* list_s = reinterpret_cast<int*>(smem + kOffList);
-  float* x_s = reinterpret_cast<float*>(smem + kOffX);
   float2* ml_s = reinterpret_cast<float2*>(smem + kOffMisc);                   // [64] (m, l)
   float* alpha_s = reinterpret_cast<float*>(smem + kOffMisc + 512);           // [64]
-  float* mxs_base = reinterpret_cast<float*>(smem + kOffMisc + 768);          // [2][4][32]
-  float* scale_s = reinterpret_cast<float*>(smem + kOffMisc + 1792);          // [64]
-  float* lpart_s = reinterpret_cast<float*>(smem + kOffMisc + 2048);          // [4][32]
-  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 2560);
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + 2624);
-  int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 2640);             // [kWarps]
+  float* scale_s = reinterpret_cast<float*>(smem + kOffMisc + 768);           // [64]
+  volatile int* flags_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 1024);
+  volatile int* stop_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 1088);   // [2][4]
+  volatile int* mv_s = reinterpret_cast<volatile int*>(smem + kOffMisc + 1120);     // [2][4]
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(smem + kOffMisc + 1152);
+  int* wcount_s = reinterpret_cast<int*>(smem + kOffMisc + 1168);             // [kWarps]
   volatile int* abort_s = flags_s + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,10 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarNever], 1);         // nothing arrives: the stall test hook waits on it
     for (int k = 0; k < 8; ++k) flags_s[k] = 0;
     fence_barrier_init();
-    // q's rope columns of this token (rows 0..h-1) as the shared-memory A operand of the
-    // rope steps
-    mbar_arrive_expect_tx(&bars[kBarQLoad], (uint32_t)(p.h * 128));
-    tma_load_3d(smem_u32(smem + kOffQRope), &tmap_qrope, 512, 0, t, &bars[kBarQLoad]);
+    // q's rope columns of this token as the shared-memory A operand of the rope steps:
+    // heads 16w..16w+15 in rows 32w..32w+15, the rows of the first-half lanes (boxes of
+    // 16 heads; heads past h read as zeros)
+    mbar_arrive_expect_tx(&bars[kBarQLoad], 4u * 16u * 128u);
+    for (int w = 0; w < 4; ++w)
+      tma_load_3d(smem_u32(smem + kOffQRope + w * 32 * 128), &tmap_qrope, 512, 16 * w, t, &bars[kBarQLoad]);
   }
   if (warp == 0) {
     tmem_alloc(tmem_base_s, kTmemCols);
@@ -237,18 +233,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, wl));
   };
 
-  // warps 0-3: running max of head `head` (log2 units; the same in the two warps of a
-  // head) and this warp's share of its running sum (the two shares are added at the end)
+  // warps 0-3: lane 16c + j of warp w serves head 16w + j and latent column half c; it
+  // keeps the head's running max (log2 units; the same in the head's two lanes) and its
+  // share of the running sum (the two lanes' shares are added at the end)
   float m_ref = -INFINITY, l_part = 0.f;
-  const int hg = warp & 1;          // head group: heads 32 hg .. 32 hg + 31
-  const int half = (warp >> 1) & 1; // latent column half of this warp's TMEM quadrant
-  const int head = 32 * hg + lane;
+  const int half = (lane >> 4) & 1;
+  const int head = 16 * (warp & 3) + (lane & 15);
   if (warp < 4) {
     // =================== softmax and O rescale (warps 0-3) ==========================
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     {
-      // q's latent columns [256 half, 256 half + 256) of head `head` into this warp's
-      // quadrant as bf16 pairs (the A operand of the latent steps); heads past h are zeros
+      // q's latent columns [256 half, 256 half + 256) of head `head` into this lane as bf16
+      // pairs (the A operand of the latent steps); heads past h are zeros
       const bool have = head < p.h;
       const uint4* qsrc =
           reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.h + (have ? head : 0)) * kDQK + 256 * half);
@@ -278,53 +274,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scale would be NaN.  For a zero scale every valid weight still rounds to exactly 1
     // (|scores * 1e-30| is far below one ulp of 1), the uniform average the definition gives.
     const float c_abs = fmaxf(fabsf(c_scale), 1e-30f);
-    const int partner = warp ^ 2;
-    const int row0 = 16 * half;         // this warp finishes tile rows row0 .. row0 + 15
-    // 16-byte slot q4 of this lane's 64-byte exchange row, rotated so a quarter warp's
-    // accesses fall in distinct banks
-    const int xrot = (lane >> 1) & 3;
-    // Warps 0-3 leave the tile loop together: warp 0 alone reads the abort flag at the top
-    // of each tile and publishes the decision before the barrier the others wait at.
+    const int row0 = 16 * half;         // this lane finishes tile rows row0 .. row0 + 15
+    // Each warp waits for its tile itself.  A wait that gives up marks the warp bad; the
+    // warps publish that at barrier B, and all four leave the loop together after barrier
+    // B of the same tile.
+    bool bad = false;
     for (int i = 0; i < n_local; ++i) {
       const int bb = i & 1;
-      if (warp == 0) {
-        bool go = !*abort_s;
-        if (go && !wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); go = false; }
-        // P buffer bb is free once P.V of tile i-2 has read it
-        if (go && i >= 2 && !wait_warp(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); go = false; }
-        if (lane == 0) flags_s[2] = go ? 0 : 1;
-      }
-      named_barrier(1, 128);   // A: the scores of tile i are in TMEM and P buffer bb is free
-      if (flags_s[2]) break;
+      if (!bad && !wait_warp(&bars[kBarSFull + bb], (i >> 1) & 1)) { fail(); bad = true; }
+      // P buffer bb is free once P.V of tile i-2 has read it
+      if (!bad && i >= 2 && !wait_warp(&bars[kBarPFree + bb], ((i >> 1) - 1) & 1)) { fail(); bad = true; }
       tc_fence_after();
-      // this quadrant's partial scores of the tile: lanes of heads 32 hg.., the 32 columns
-      // of its column half (first half: columns 0-31, second half: columns 32-63)
-      uint32_t v[32];
-      tmem_ld32(lane_base + kColS + 64 * bb + 32 * half, v);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarSFree + bb]);
-      {
-        // the partner finishes the other 16 rows: send it this half's partials of them
-        const int snd = half ? 0 : 16;
-        float* dst = x_s + warp * kXWarpFloats + lane * 16;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4*>(dst + 4 * (q4 ^ xrot)) =
-              make_uint4(v[snd + 4 * q4], v[snd + 4 * q4 + 1], v[snd + 4 * q4 + 2], v[snd + 4 * q4 + 3]);
-      }
-      named_barrier(4 + hg, 64);   // X: the two halves' partials of this head group are published
+      // The tile's 64 score columns of this quadrant: a first-half lane's partials are in
+      // columns 0-31 (rows 0-31), a second-half lane's in columns 32-63.  Each lane keeps
+      // its half's partials of its own 16 rows and passes those of the other 16 rows to the
+      // head's other lane.
       float s[16];
       {
-        const float* src = x_s + partner * kXWarpFloats + lane * 16;
+        uint32_t c0[16], c1[16], c2[16], c3[16];
+        const uint32_t sb = lane_base + kColS + 64 * bb;
+        tmem_ld16(sb, c0);
+        tmem_ld16(sb + 16, c1);
+        tmem_ld16(sb + 32, c2);
+        tmem_ld16(sb + 48, c3);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kBarSFree + bb]);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 y = *reinterpret_cast<const uint4*>(src + 4 * (q4 ^ xrot));
-          s[4 * q4] = __uint_as_float(v[row0 + 4 * q4]) + __uint_as_float(y.x);
-          s[4 * q4 + 1] = __uint_as_float(v[row0 + 4 * q4 + 1]) + __uint_as_float(y.y);
-          s[4 * q4 + 2] = __uint_as_float(v[row0 + 4 * q4 + 2]) + __uint_as_float(y.z);
-          s[4 * q4 + 3] = __uint_as_float(v[row0 + 4 * q4 + 3]) + __uint_as_float(y.w);
+        for (int j = 0; j < 16; ++j) {
+          const float own = __uint_as_float(half ? c3[j] : c0[j]);
+          const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(half ? c2[j] : c1[j]), 16);
+          s[j] = own + other;
         }
       }
       const int g = (int)crank + (int)G * i;   // the unit's tile index
@@ -338,14 +319,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = s[0];
 #pragma unroll
       for (int j = 1; j < 16; ++j) mx = fmaxf(mx, s[j]);
-      float* mx_s = mxs_base + 128 * bb;   // [4 warps][32 heads] of this tile parity
-      mx_s[warp * 32 + lane] = mx;
-      named_barrier(2, 128);   // B: every warp's partial max of tile i is published
-      // the same maximum in both warps of a head: fmaxf is exact and symmetric
-      const float mt = fmaxf(mx_s[hg * 32 + lane], mx_s[(hg + 2) * 32 + lane]) * c_abs;
+      // the tile max of the head: fmaxf is exact and symmetric, both lanes see the same
+      const float mt = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * c_abs;
       float m_new = m_ref;
       if (head < p.h && (i == 0 || mt > m_ref + kRescaleThreshold)) m_new = fmaxf(mt, m_ref);
       const float alpha = (i == 0 || head >= p.h) ? 1.f : ex2(m_ref - m_new);
+      const bool moved = __any_sync(0xffffffffu, i > 0 && m_new != m_ref);
       m_ref = m_new;
       uint32_t pk[8];
       float sm = 0.f;
@@ -367,32 +346,37 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         fence_proxy_async_smem();
       }
-      // O is rescaled (rarely: the reference max moves only by more than the threshold)
-      // once P.V of the previous tile has completed.  A warp that rescales one of its
-      // heads waits for that itself; the barrier below passes the ordering to the others.
-      // (Tile i+1 waits on the same phase of that buffer again: it cannot have moved on,
-      // P.V of tile i+1 is not issued yet.)
-      const bool resc_w = __any_sync(0xffffffffu, alpha != 1.f);
-      if (resc_w && i >= 1 && !wait_warp(&bars[kBarPFree + (bb ^ 1)], ((i - 1) >> 1) & 1)) fail();
-      if (half == 0) alpha_s[head] = alpha;
-      if (lane == 0) flags_s[4 + warp] = resc_w ? 1 : 0;
-      named_barrier(3, 128);   // C: whether O is rescaled, and by what
-      if ((flags_s[4] | flags_s[5] | flags_s[6] | flags_s[7]) && !*abort_s) {
-        tc_fence_after();
-        // O^T lane v holds output column v of every head: scale column hh by alpha[hh]
+      if (lane == 0) {
+        stop_s[4 * bb + warp] = bad ? 1 : 0;
+        mv_s[4 * bb + warp] = moved ? 1 : 0;
+      }
+      named_barrier(2, 128);   // B: whether any warp gave up, and whether any head's max moved
+      if (stop_s[4 * bb] | stop_s[4 * bb + 1] | stop_s[4 * bb + 2] | stop_s[4 * bb + 3]) break;
+      if (mv_s[4 * bb] | mv_s[4 * bb + 1] | mv_s[4 * bb + 2] | mv_s[4 * bb + 3]) {
+        // Rare: some head's reference max moved by more than the threshold.  Every warp
+        // rescales its output-column lanes of O for all heads, once P.V of the previous tile
+        // has completed.  (Tile i+1 waits on the same phase of that buffer again: it cannot
+        // have moved on, P.V of tile i+1 is not issued yet.)
+        if (lane < 16) alpha_s[head] = alpha;
+        if (!bad && !wait_warp(&bars[kBarPFree + (bb ^ 1)], ((i - 1) >> 1) & 1)) { fail(); bad = true; }
+        named_barrier(3, 128);   // C: the factors are published
+        if (!bad) {
+          tc_fence_after();
+          // O^T lane v holds output column v of every head: scale column hh by alpha[hh]
 #pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
+          for (int m = 0; m < 4; ++m) {
 #pragma unroll
-          for (int c16 = 0; c16 < kNH / 16; ++c16) {
-            uint32_t o[16];
-            tmem_ld16(lane_base + kColO + kNH * m + 16 * c16, o);
-            tmem_ld_wait();
+            for (int c16 = 0; c16 < kNH / 16; ++c16) {
+              uint32_t o[16];
+              tmem_ld16(lane_base + kColO + kNH * m + 16 * c16, o);
+              tmem_ld_wait();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[16 * c16 + k]);
-            tmem_st16(lane_base + kColO + kNH * m + 16 * c16, o);
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha_s[16 * c16 + k]);
+              tmem_st16(lane_base + kColO + kNH * m + 16 * c16, o);
+            }
           }
+          tmem_st_wait();
         }
-        tmem_st_wait();
       }
       tc_fence_before();
       __syncwarp();
@@ -526,18 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       have_o = wait_warp(&bars[kBarPvFinal], 0);
       if (!have_o) fail();
     }
-    lpart_s[warp * 32 + lane] = l_part;
-    named_barrier(2, 128);
-    if (warp < 2) {
-      // head 32 warp + lane: its sum is the two column-half warps' shares
-      const float l_sum = lpart_s[warp * 32 + lane] + lpart_s[(warp + 2) * 32 + lane];
-      ml_s[head] = (have_o && head < p.h) ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
-    }
+    // the head's sum is its two lanes' shares
+    const float l_sum = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+    if (lane < 16) ml_s[head] = (have_o && head < p.h) ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.f);
   }
   tc_fence_before();
   cluster_sync();   // every CTA's (m, l) is published
   tc_fence_after();
-  if (warp < 2) {
+  if (warp < 4 && lane < 16) {
     // head `head`: the merged max M, total sum L and this CTA's weight exp2(m - M) / L
     float M = -INFINITY;
     for (uint32_t c = 0; c < G; ++c) {

@@ -774,9 +774,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int kernel_id, cudaStream_t 
   if (kernel_id == 2 || kernel_id == 3) {
     // whole rows as nine 64-column SW128 boxes from one map; q's rope columns as one box
     CUtensorMap rows, qrope;
+    // (the stacked-half kernel loads q's rope rows 16 heads at a time)
     const bool ok_h = kernel_id == 2 ? narrow_supports(p.h) : stack_supports(p.h);
     if (!ok_h || !make_row_map(&rows, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_q_map(&qrope, p.q, p.h, T, p.h, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_q_map(&qrope, p.q, p.h, T, kernel_id == 2 ? p.h : 16, 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     return kernel_id == 2 ? launch_decode_narrow(p, rows, qrope, stream)
                           : launch_decode_stack(p, rows, qrope, device_sm_count(), stream);
