@@ -128,12 +128,13 @@ cudaError_t prepare_decode_narrow();
 int narrow_cluster_size(long long units, int n_sms);
 cudaError_t launch_decode_narrow(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
                                  cudaStream_t stream);
-// the stacked-half kernel (sfa_stack.cu, 33 <= h <= 64): the same maps, one CTA (or a
-// cluster of 2 or 4 when units are few) per unit
+// the stacked-half kernel (sfa_stack.cu, 33 <= h <= 64): the same maps (q's rope map with
+// boxes of 16 heads) and the output map (32 columns x h heads), one CTA (or a cluster of
+// 2 or 4 when units are few) per unit
 bool stack_supports(int h);
 cudaError_t prepare_decode_stack();
 cudaError_t launch_decode_stack(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
-                                int n_sms, cudaStream_t stream);
+                                const CUtensorMap& out_map, int n_sms, cudaStream_t stream);
 // SM count of the current device (looked up once per device)
 int device_sm_count();
 

@@ -517,6 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_barrier(2, 128);
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const int v = warp * 32 + lane;   // TMEM lane: output column v of each 128-column block
+    // the heads' output scales in registers: read from shared memory between the stores
+    // below, each would wait for the stores before it
+    float sc[NH];
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) sc[hh] = scale_s[hh];
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
       uint32_t o[NH];
@@ -535,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c4 = 0; c4 < NH / 4; ++c4) {
         const int sw = c4 ^ (v & (NH / 4 - 1));
-        st_cluster_v4(dst + 16u * sw, __float_as_uint(__uint_as_float(o[4 * c4]) * scale_s[4 * c4]),
-                      __float_as_uint(__uint_as_float(o[4 * c4 + 1]) * scale_s[4 * c4 + 1]),
-                      __float_as_uint(__uint_as_float(o[4 * c4 + 2]) * scale_s[4 * c4 + 2]),
-                      __float_as_uint(__uint_as_float(o[4 * c4 + 3]) * scale_s[4 * c4 + 3]));
+        st_cluster_v4(dst + 16u * sw, __float_as_uint(__uint_as_float(o[4 * c4]) * sc[4 * c4]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 1]) * sc[4 * c4 + 1]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 2]) * sc[4 * c4 + 2]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 3]) * sc[4 * c4 + 3]));
       }
     }
   }

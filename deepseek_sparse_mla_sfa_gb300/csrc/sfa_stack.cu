@@ -114,7 +114,7 @@ struct StackParams {
 template <bool kInterleaved>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_stack_kernel(const __grid_constant__ CUtensorMap tmap_rows, const __grid_constant__ CUtensorMap tmap_qrope,
-                        const StackParams sp) {
+                        const __grid_constant__ CUtensorMap tmap_out, const StackParams sp) {
   const DecodeParams& p = sp.p;
   extern __shared__ char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmap_rows);
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_out);
 
   // ---- index resolution: count per warp chunk, then ordered compaction into smem ----
   const int chunk = ((p.top_k + kWarps * 32 - 1) / (kWarps * 32)) * 32;
@@ -538,15 +539,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (crank == 0 && head < p.h && !*abort_s)
       p.lse[((size_t)r * T + t) * p.h + head] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : -INFINITY;
   }
-  float* outp = p.out + ((size_t)r * T + t) * p.h * kDV;
   const int v = warp * 32 + lane;   // TMEM lane of warps 0-3: output column v of each 128-column block
-  // the merge buffer (in the idle stages): for block m, owner m % G, slot of source CTA c:
-  //   recv[((c * (4 / G) + m / G) * 128 + v) * 64 + hh], 16-byte chunks swizzled by v
+  // The output leaves through TMA tensor stores of 32-column x h-head boxes staged in the
+  // idle stages: box (m, c) holds output columns 128m + 32c .. +31 of every head, one
+  // 128-byte SW128 row per head, so warp c of the softmax warps fills box (m, c) with one
+  // conflict-free 128-byte row store per head.
+  auto stage_box = [&](char* box, int hh, float x) {
+    *reinterpret_cast<float*>(box + hh * 128 + ((((lane >> 2) ^ (hh & 7)) << 4) | ((lane & 3) << 2))) = x;
+  };
+  const int out_tok = r * T + t;   // token row of out (or of the shard's partials)
+  // the merge buffer (G > 1, in the idle stages): for block m, owner m % G, slot of source
+  // CTA c: recv[((c * (4 / G) + m / G) * 128 + v) * 64 + hh], 16-byte chunks swizzled by v;
+  // the owner's boxes follow it
   float* recv = reinterpret_cast<float*>(smem);
   const int blocks_per = 4 / (int)G;
+  char* staging = smem + (G == 1 ? 0 : 4 * 128 * kNH * 4);
+  static_assert(4 * 128 * kNH * 4 + 2 * 4 * kNH * 128 <= kOffP, "merge buffer and boxes stay below P");
   if (warp < 4) {
     named_barrier(2, 128);
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    // the heads' output scales in registers: read from shared memory between the staging
+    // stores below, each would wait for the stores before it
+    float sc[kNH];
+#pragma unroll
+    for (int hh = 0; hh < kNH; ++hh) sc[hh] = scale_s[hh];
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
       uint32_t o[kNH];
@@ -560,11 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kNH; ++k) o[k] = 0u;
       }
       if (G == 1) {
-        // the whole output is this CTA's: one coalesced 128-byte row segment per (head, warp)
         if (!*abort_s) {
+          char* box = staging + (4 * m + warp) * (kNH * 128);
 #pragma unroll
-          for (int hh = 0; hh < kNH; ++hh)
-            if (hh < p.h) outp[(size_t)hh * kDV + 128 * m + v] = __uint_as_float(o[hh]) * scale_s[hh];
+          for (int hh = 0; hh < kNH; ++hh) stage_box(box, hh, __uint_as_float(o[hh]) * sc[hh]);
         }
         continue;
       }
@@ -574,19 +589,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c4 = 0; c4 < kNH / 4; ++c4) {
         const int sw = c4 ^ (v & (kNH / 4 - 1));
-        st_cluster_v4(dst + 16u * sw, __float_as_uint(__uint_as_float(o[4 * c4]) * scale_s[4 * c4]),
-                      __float_as_uint(__uint_as_float(o[4 * c4 + 1]) * scale_s[4 * c4 + 1]),
-                      __float_as_uint(__uint_as_float(o[4 * c4 + 2]) * scale_s[4 * c4 + 2]),
-                      __float_as_uint(__uint_as_float(o[4 * c4 + 3]) * scale_s[4 * c4 + 3]));
+        st_cluster_v4(dst + 16u * sw, __float_as_uint(__uint_as_float(o[4 * c4]) * sc[4 * c4]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 1]) * sc[4 * c4 + 1]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 2]) * sc[4 * c4 + 2]),
+                      __float_as_uint(__uint_as_float(o[4 * c4 + 3]) * sc[4 * c4 + 3]));
+      }
+    }
+    if (G == 1) {
+      fence_proxy_async_smem();
+      named_barrier(2, 128);   // every box is staged
+      if (threadIdx.x == 0 && !*abort_s) {
+        for (int b = 0; b < 16; ++b)
+          tma_store_3d(&tmap_out, smem_u32(staging + b * (kNH * 128)), 32 * b, 0, out_tok);
+        bulk_commit_group();
+        bulk_wait_read<0>();   // shared memory may be released once read; the writes finish with the grid
       }
     }
   }
   tc_fence_before();
   cluster_sync();   // every CTA's scaled partial O has landed with its owner
   tc_fence_after();
-  if (G > 1 && warp < 4 && !*abort_s) {
-    // this CTA's output blocks: the sum of the G scaled partials
-    for (int m = (int)crank; m < 4; m += (int)G) {
+  if (G > 1 && warp < 4) {
+    // this CTA's output blocks: the sum of the G scaled partials, staged as boxes
+    int nb = 0;
+    for (int m = (int)crank; m < 4; m += (int)G, ++nb) {
       float acc[kNH];
 #pragma unroll
       for (int k = 0; k < kNH; ++k) acc[k] = 0.f;
@@ -598,9 +624,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[4 * c4] += x.x; acc[4 * c4 + 1] += x.y; acc[4 * c4 + 2] += x.z; acc[4 * c4 + 3] += x.w;
         }
       }
+      char* box = staging + (4 * nb + warp) * (kNH * 128);
 #pragma unroll
-      for (int hh = 0; hh < kNH; ++hh)
-        if (hh < p.h) outp[(size_t)hh * kDV + 128 * m + v] = acc[hh];
+      for (int hh = 0; hh < kNH; ++hh) stage_box(box, hh, acc[hh]);
+    }
+    fence_proxy_async_smem();
+    named_barrier(2, 128);   // every owned box is staged
+    if (threadIdx.x == 0 && !*abort_s) {
+      int k = 0;
+      for (int m = (int)crank; m < 4; m += (int)G, ++k)
+        for (int c = 0; c < 4; ++c)
+          tma_store_3d(&tmap_out, smem_u32(staging + (4 * k + c) * (kNH * 128)), 128 * m + 32 * c, 0, out_tok);
+      bulk_commit_group();
+      bulk_wait_read<0>();
     }
   }
 
@@ -636,7 +672,7 @@ cudaError_t prepare_decode_stack() {
 }
 
 cudaError_t launch_decode_stack(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
-                                int n_sms, cudaStream_t stream) {
+                                const CUtensorMap& out_map, int n_sms, cudaStream_t stream) {
   const long long T = (long long)p.B * p.Q;
   const long long units = T * p.n_splits;
   if (units == 0) return cudaSuccess;
@@ -663,7 +699,7 @@ cudaError_t launch_decode_stack(const DecodeParams& p, const CUtensorMap& rows_m
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, rows_map, qrope_map, sp);
+  e = cudaLaunchKernelEx(&cfg, kernel, rows_map, qrope_map, out_map, sp);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

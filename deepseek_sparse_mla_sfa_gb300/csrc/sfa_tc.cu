@@ -779,8 +779,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int kernel_id, cudaStream_t 
     if (!ok_h || !make_row_map(&rows, p.kv, (int)num_rows, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_q_map(&qrope, p.q, p.h, T, kernel_id == 2 ? p.h : 16, 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    return kernel_id == 2 ? launch_decode_narrow(p, rows, qrope, stream)
-                          : launch_decode_stack(p, rows, qrope, device_sm_count(), stream);
+    if (kernel_id == 2) return launch_decode_narrow(p, rows, qrope, stream);
+    CUtensorMap omap;
+    if (!make_out_map(&omap, p.out, p.h, T * p.n_splits, p.h)) return cudaErrorInvalidValue;
+    return launch_decode_stack(p, rows, qrope, omap, device_sm_count(), stream);
   }
   TcParams tp;
   tp.p = p;
