@@ -196,9 +196,12 @@ sfa_status sfa_decode_ex(const void* q, const void* kv, const int32_t* block_tab
     if ((out && !lse) || (!out && lse)) return SFA_ERR_INVALID_ARG;
     if (merge_after && (!aligned(out, 16) || !aligned(lse, 4))) return SFA_ERR_INVALID_ARG;
   }
+  // the workspace is optional: without enough of it the kernels use a schedule that needs none
   const size_t need = sfa_decode_workspace_bytes(B, Q, h, top_k, n_splits);
-  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 256)))
-    return SFA_ERR_WORKSPACE;
+  if (need == 0 || !workspace || workspace_bytes < need || !aligned(workspace, 256)) {
+    workspace = nullptr;
+    workspace_bytes = 0;
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SFA_ERR_CUDA;

@@ -132,6 +132,9 @@ cudaError_t launch_decode_narrow(const DecodeParams& p, const CUtensorMap& rows_
 // boxes of 16 heads) and the output map (32 columns x h heads), one CTA (or a cluster of
 // 2 or 4 when units are few) per unit
 bool stack_supports(int h);
+// workspace that lets the stacked-half kernel balance `units` units over n_sms SMs (0 when
+// it would not: other head counts, or no more units than SMs)
+size_t stack_workspace_bytes(long long units, int h, int top_k, int n_sms);
 cudaError_t prepare_decode_stack();
 cudaError_t launch_decode_stack(const DecodeParams& p, const CUtensorMap& rows_map, const CUtensorMap& qrope_map,
                                 const CUtensorMap& out_map, int n_sms, cudaStream_t stream);

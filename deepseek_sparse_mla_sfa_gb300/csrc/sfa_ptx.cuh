@@ -189,6 +189,13 @@ __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, const void* sr
       "r"(smem_u32(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+// bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from global memory
+// into this CTA's shared memory, completing on `bar`
+__device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until the sources of all but `n` most recent bulk groups have been read
 template <int n>

@@ -742,8 +742,8 @@ bool tc_supports_ptrs(const void* q, const void* kv, const void* out) {
 }
 
 size_t tc_workspace_bytes(int T, int h, int top_k, int n_splits) {
-  (void)T; (void)h; (void)top_k; (void)n_splits;
-  return 0;
+  // only the stacked-half kernel uses scratch: its balanced schedule
+  return stack_workspace_bytes((long long)T * n_splits, h, top_k, device_sm_count());
 }
 
 int tc_launches(int T, int h, int top_k, int n_splits) {

@@ -93,11 +93,12 @@ typedef void *sfa_stream; /* a cudaStream_t */
  *               into them on the same stream (as sfa_lse_merge does).
  *   out_part, lse_part  device, fp32 [n_splits, B*Q, h, 512] and [n_splits, B*Q, h];
  *               required when n_splits > 1, ignored otherwise.
- *   workspace   reserved: device scratch of at least sfa_decode_workspace_bytes(...)
- *               bytes, 256-byte aligned.  That size is 0 for every shape the current
- *               kernels accept, so callers may pass NULL and 0; the argument keeps the
- *               ABI stable for a kernel that needs scratch.  Contents need no
- *               initialisation and are undefined afterwards.
+ *   workspace   optional device scratch, 256-byte aligned.  With at least
+ *               sfa_decode_workspace_bytes(...) bytes the kernel for 33-64 heads
+ *               spreads the work of more (token, shard) units than SMs evenly over
+ *               the SMs; with less (or NULL) the call runs all the same, one unit per
+ *               SM at a time.  Contents need no initialisation and are undefined
+ *               afterwards; calls that overlap on the GPU must not share it.
  *   All float/bf16 buffers must be 16-byte aligned.
  * Returns SFA_OK, or an error code with nothing launched.
  */
@@ -109,9 +110,12 @@ sfa_status sfa_decode(const void *q, const void *kv, const int32_t *block_table,
                       sfa_stream stream);
 
 /*
- * sfa_decode_workspace_bytes -- device scratch sfa_decode needs for this shape.
- * Reserved: 0 for every shape the current kernels accept (no kernel of this
- * library uses scratch beyond its inputs and outputs).
+ * sfa_decode_workspace_bytes -- device scratch that lets sfa_decode balance this
+ * shape over the SMs of the current device (see `workspace` above).  Nonzero only
+ * when 33 <= h <= 64 and B*Q*n_splits exceeds the SM count: then 2 partial
+ * results (64 x 512 fp32 and 64 (max, sum) pairs) per SM, plus one counter per
+ * (token, shard) unit, each part rounded up to 256 bytes.  0 otherwise, and 0
+ * while sfa_set_kernel_path selects a fixed kernel.
  */
 size_t sfa_decode_workspace_bytes(int B, int Q, int h, int top_k, int n_splits);
 

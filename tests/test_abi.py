@@ -89,10 +89,22 @@ def test_stall_injection_hook_roundtrip(lib):
     assert lib.sfa_set_stall_injection(0) == old
 
 
-def test_workspace_is_reserved_and_zero(lib):
-    # no kernel of the library uses scratch: the reserved workspace size is 0 everywhere
-    for args in ((64, 1, 128, 2048, 1), (32, 1, 128, 2048, 8), (128, 2, 64, 2048, 1), (32, 1, 16, 8192, 4)):
-        assert lib.sfa_decode_workspace_bytes(*args) == 0
+def test_workspace_only_for_the_balanced_schedule(lib):
+    # scratch is used only by the 33-64-head kernel when its (token, shard) units outnumber
+    # the SMs: two 64 x 512 fp32 partials and 64 (max, sum) pairs per SM plus a counter per
+    # unit, each part rounded up to 256 bytes
+    for args in ((64, 1, 128, 2048, 1), (32, 1, 128, 2048, 8), (32, 1, 16, 8192, 4), (8, 1, 64, 2048, 1),
+                 (300, 1, 32, 2048, 1), (300, 1, 65, 2048, 1), (300, 1, 64, 0, 1)):
+        assert lib.sfa_decode_workspace_bytes(*args) == 0, args
+    ws = lib.sfa_decode_workspace_bytes(128, 2, 64, 2048, 1)
+    per_sm = 2 * (64 * 512 * 4 + 64 * 8)
+    counters = (256 * 4 + 255) // 256 * 256
+    assert ws > 0 and ws % 256 == 0 and (ws - counters) % per_sm == 0
+    n_sms = (ws - counters) // per_sm
+    assert 1 <= n_sms < 256
+    # the same for 33 heads and for shards as units
+    assert lib.sfa_decode_workspace_bytes(128, 2, 33, 2048, 1) == ws
+    assert lib.sfa_decode_workspace_bytes(64, 1, 48, 2048, 4) == ws
 
 
 def _noalloc(lib, out, lse, **kw):

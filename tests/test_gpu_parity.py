@@ -58,6 +58,13 @@ SMALL = [
     W("h128_groups2_dcp", B=30, Q=1, h=128, S=20000, recent=2000, top_k=512, n_splits=8,
       index_kind="dcp_long", seed=47),
     W("h64_groups_mtp", B=20, Q=2, h=64, S=6000, S_min=40, top_k=700, n_splits=3, index_kind="causal", seed=48),
+    # 33-64 heads with more (token, shard) units than SMs: balanced ranges of tiles, units cut
+    # between two CTAs and merged through the workspace; ragged lists, short sequences, and
+    # shards (many of them empty) as units
+    W("h40_balanced", B=80, Q=2, h=40, S=2000, S_min=20, top_k=300, n_splits=1, index_kind="causal", seed=49),
+    W("h64_balanced_shards", B=45, Q=1, h=64, S=3000, top_k=333, n_splits=4, index_kind="uniform", seed=50),
+    W("h48_balanced_dcp", B=40, Q=1, h=48, S=12000, recent=1500, top_k=257, n_splits=8,
+      index_kind="dcp_long", seed=51),
 ]
 
 # which kernel decode_launches reports per kernel-path setting (0 automatic, 1 CUDA-core,
