@@ -386,7 +386,8 @@ def run_ours(args, world, rank, local):
                    "frac_of_burst": value / world / peaks["bf16_tflops"],
                    "frac_of_sustained": value / world / peaks["bf16_tflops_sustained"],
                    "peak_burst": peaks["bf16_tflops"], "peak_sustained": peaks["bf16_tflops_sustained"]},
-        "kernel_path": {2: "tcgen05 small-head", 1: "tcgen05 CTA pair", 0: "cuda-core"}[tc_path],
+        "kernel_path": {3: "tcgen05 stacked-half", 2: "tcgen05 small-head", 1: "tcgen05 CTA pair",
+                        0: "cuda-core"}[tc_path],
         "kernels": {"decode_ms": dec_avg, "lse_merge_ms": mrg_avg if n > 1 else None},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -581,7 +582,7 @@ def read_traffic(kernel: str, tc_path: int, workload: str):
     if not os.path.exists(path):
         return None
     from deepseek_sparse_mla_sfa_gb300 import build as _b
-    src = {"decode": {2: "sfa_narrow.cu", 1: "sfa_tc.cu", 0: "sfa_simt.cu"}[int(tc_path)],
+    src = {"decode": {3: "sfa_stack.cu", 2: "sfa_narrow.cu", 1: "sfa_tc.cu", 0: "sfa_simt.cu"}[int(tc_path)],
            "lse_merge": "sfa_merge.cu"}.get(kernel)
     if src is None:
         return None
@@ -668,12 +669,17 @@ def main():
                     help="skip timing the other workloads (the line's `configs` object)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's B (smaller cases for profiler captures)")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override the workload's S (smaller caches for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.batch:
-        w = dataclasses.replace(workloads.CONFIGS[args.config], B=args.batch,
-                                name=f"{args.config}_b{args.batch}")
+    if args.batch or args.seq_len:
+        base = workloads.CONFIGS[args.config]
+        S = args.seq_len or base.S
+        w = dataclasses.replace(base, B=args.batch or base.B, S=S, S_min=min(base.S_min, S) if base.S_min else 0,
+                                top_k=min(base.top_k, S),
+                                name=f"{args.config}_b{args.batch or base.B}_s{S}")
         workloads.CONFIGS[w.name] = w
         args.config = w.name
     world_env = int(os.environ.get("WORLD_SIZE", "1"))
