@@ -365,6 +365,31 @@ def test_small_head_kernel_timeout_is_reported_and_context_survives(h, B):
     assert sfa.last_device_status() == 0
 
 
+@pytest.mark.parametrize("B,Q", [(2, 1), (40, 1), (100, 2)])
+def test_stacked_kernel_timeout_is_reported_and_context_survives(B, Q):
+    # the 33-64-head kernel with a stalled wait: clusters of 4 (B=2), clusters of 2 (B=40)
+    # and balanced ranges of tiles over the SMs (200 units): it reports the timeout, every
+    # warp leaves its loop, and the next call is exact (the cut units' counters cleared)
+    w = W("timeout_stack", B=B, Q=Q, h=64, S=4096, S_min=600 if Q > 1 else 0, top_k=512, n_splits=1,
+          index_kind="causal" if Q > 1 else "uniform", seed=32)
+    inp = workloads.make(w, device="cuda")
+    assert sfa.decode_launches(w.B, w.Q, w.h, w.top_k, w.block_size, w.n_splits)[1] == 3
+    sfa.last_device_status()
+    prev = sfa.set_wait_limit(1000)
+    prev_stall = sfa.set_stall_injection(True)
+    try:
+        run_cuda(inp)
+        status = sfa.last_device_status()
+    finally:
+        sfa.set_stall_injection(prev_stall)
+        sfa.set_wait_limit(prev)
+    assert status == -5
+    ro, rl = oracle.decode(problem_of(inp))
+    out, lse = run_cuda(inp)
+    compare(out, lse, ro, rl, "stacked kernel after timeout")
+    assert sfa.last_device_status() == 0
+
+
 def test_one_poll_wait_cap_reports_or_completes():
     # a cap of one poll may or may not see each barrier complete in time; either way the
     # kernel must return, and the next call is exact
