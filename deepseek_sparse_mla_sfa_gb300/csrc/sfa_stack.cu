@@ -697,6 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // This CTA has no further piece, so its stages are idle: the tail's rows come in
             // by bulk copies, and this piece's O is still in TMEM.
             if (threadIdx.x == 0) {
+              // The tail's partial was written by another CTA's generic-proxy stores and is
+              // now visible to this thread (the counter's fences); the bulk copies read it
+              // through the async proxy, which a proxy fence orders after that.
+              asm volatile("fence.proxy.async.global;" ::: "memory");
               const uint32_t bytes = (uint32_t)p.h * kDV * 4;
               mbar_arrive_expect_tx(&bars[kBarMerge], bytes);
               for (uint32_t o = 0; o < bytes; o += 32768u)
