@@ -38,6 +38,12 @@ INTERLEAVED = [
     # more (token, shard) pairs than CTA pairs: the CTA-pair kernel takes groups of shards
     (W("il_h128_groups", B=20, Q=1, h=128, S=8000, top_k=600, n_splits=8, index_kind="uniform",
        seed=36), [16, 1000]),
+    # 33-64 heads: more (token, shard) units than SMs (balanced ranges of tiles, units cut
+    # between two CTAs), and few units (clusters of 4 CTAs sharing each unit)
+    (W("il_h64_balanced", B=90, Q=2, h=64, S=3000, S_min=300, top_k=256, n_splits=2, index_kind="causal",
+       seed=37), [16, 100]),
+    (W("il_h40_clusters", B=3, Q=1, h=40, S=2000, top_k=500, n_splits=4, index_kind="uniform",
+       seed=38), [1, 64]),
 ]
 CASES = [(w, g) for w, gs in INTERLEAVED for g in gs]
 
@@ -91,6 +97,9 @@ PER_TOKEN = [
     # more than 2048 valid entries: the tensor-core kernel refills its resolved list
     W("bt_h128_q2_k3000", B=1, Q=2, h=128, S=8192, S_min=4000, top_k=3000, n_splits=1, index_kind="causal",
       seed=44),
+    # 33-64 heads with more units than SMs: balanced ranges of tiles
+    W("bt_h48_balanced", B=80, Q=2, h=48, S=2500, S_min=200, top_k=200, n_splits=1, index_kind="causal",
+      seed=45),
 ]
 
 
